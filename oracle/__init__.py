@@ -1,0 +1,264 @@
+"""CPU oracle for the lowbias32 counter-based random fills.
+
+TEST INFRASTRUCTURE ONLY.  The tests, the package's ``smoke()`` check and the
+benchmark's CPU-baseline leg are the only users; the product path never
+imports this package.  ``oracle.c`` holds the arithmetic (plain C, one element
+at a time); this module only compiles it with gcc and marshals numpy arrays
+through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import platform
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _build/liboracle.so (if stale) and return its path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off",
+           "-fexcess-precision=standard", "-fno-fast-math", "-fPIC", "-shared",
+           _SRC, "-o", _LIB + ".tmp", "-lm"]
+    if platform.machine() in ("x86_64", "AMD64"):
+        cmd.append("-lquadmath")
+    subprocess.run(cmd, check=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+_u32, _u64, _i32, _i64 = C.c_uint32, C.c_uint64, C.c_int32, C.c_int64
+_sz, _f32, _f64, _p = C.c_size_t, C.c_float, C.c_double, C.c_void_p
+
+_SIGS = {
+    "orc_hash32": (_u32, [_u32]),
+    "orc_draw32": (_u32, [_u32, _u32]),
+    "orc_draw64": (_u64, [_u32, _u32]),
+    "orc_uniform_f32": (_f32, [_u32, _u32]),
+    "orc_uniform_f64": (_f64, [_u32, _u32]),
+    "orc_lemire_step": (C.c_int, [_u64, _u64, C.c_uint, C.POINTER(_u64)]),
+    "orc_below32": (_u32, [_u32, _u32, _u32]),
+    "orc_below64": (_u64, [_u32, _u32, _u64]),
+    "orc_randn": (_f64, [_u32, _u32]),
+    "orc_dropout": (_f32, [_f32, _f32, _u32, _u32]),
+    "orc_zexp": (_f64, [_f64]),
+    "orc_zlog": (_f64, [_f64]),
+    "orc_zig_table": (C.c_int, [C.c_uint, _p, _p, C.POINTER(_f64), C.POINTER(_f64)]),
+    "orc_zig1024": (None, [_p, _p]),
+    "orc_zig_first_draw_fast": (C.c_int, [_u32, _u32]),
+    "orc_normal_f64": (_f64, [_u32, _u32]),
+    "orc_fill_u32": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_u64": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_f32": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_f64": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_u32_below": (None, [_u32, _u32, _sz, _p, _u32, _p]),
+    "orc_fill_u64_below": (None, [_u32, _u32, _sz, _p, _u64, _p]),
+    "orc_fill_i32_range": (None, [_u32, _u32, _sz, _p, _i32, _u32, _p]),
+    "orc_fill_i64_range32": (None, [_u32, _u32, _sz, _p, _i64, _u32, _p]),
+    "orc_fill_i64_range": (None, [_u32, _u32, _sz, _p, _i64, _u64, _p]),
+    "orc_fill_randn": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_normal_f64": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_dropout_fill": (None, [_p, _f32, _u32, _u32, _sz, _p, _p]),
+    "orc_fill_zig_fast": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_zexp_fill": (None, [_p, _sz, _p]),
+    "orc_zlog_fill": (None, [_p, _sz, _p]),
+}
+
+
+def _bind(handle: C.CDLL) -> C.CDLL:
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
+def compile_variant(source_text: str, out_dir: str) -> str:
+    """Compile a modified copy of oracle.c (used by the tests that plant a
+    mistake in the oracle and check that a pin catches it)."""
+    src = os.path.join(out_dir, "oracle_variant.c")
+    so = os.path.join(out_dir, "liboracle_variant.so")
+    with open(src, "w") as fh:
+        fh.write(source_text)
+    cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off",
+           "-fexcess-precision=standard", "-fno-fast-math", "-fPIC", "-shared",
+           src, "-o", so, "-lm"]
+    if platform.machine() in ("x86_64", "AMD64"):
+        cmd.append("-lquadmath")
+    subprocess.run(cmd, check=True)
+    return so
+
+
+def source() -> str:
+    with open(_SRC) as fh:
+        return fh.read()
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data
+
+
+def _idx(n: int | None, idx) -> tuple[int, np.ndarray | None]:
+    if idx is None:
+        return int(n), None
+    idx = np.ascontiguousarray(idx, dtype=np.uint64)
+    return idx.size, idx
+
+
+class Oracle:
+    """numpy front end over one loaded copy of the oracle library."""
+
+    def __init__(self, path: str):
+        self.lib = _bind(C.CDLL(path))
+
+    # Scalar definitions ------------------------------------------------------
+    def hash32(self, x: int) -> int:
+        return self.lib.orc_hash32(x & 0xFFFFFFFF)
+
+    def draw32(self, seed: int, c: int) -> int:
+        return self.lib.orc_draw32(seed & 0xFFFFFFFF, c & 0xFFFFFFFF)
+
+    def draw64(self, seed: int, c: int) -> int:
+        return self.lib.orc_draw64(seed & 0xFFFFFFFF, c & 0xFFFFFFFF)
+
+    def lemire_step(self, x: int, b: int, w: int) -> tuple[bool, int]:
+        v = C.c_uint64()
+        ok = self.lib.orc_lemire_step(x, b, w, C.byref(v))
+        return bool(ok), v.value
+
+    def below32(self, seed: int, c: int, b: int) -> int:
+        return self.lib.orc_below32(seed & 0xFFFFFFFF, c & 0xFFFFFFFF, b)
+
+    def below64(self, seed: int, c: int, b: int) -> int:
+        return self.lib.orc_below64(seed & 0xFFFFFFFF, c & 0xFFFFFFFF, b)
+
+    def randn(self, seed: int, c: int) -> float:
+        return self.lib.orc_randn(seed & 0xFFFFFFFF, c & 0xFFFFFFFF)
+
+    def normal_f64(self, seed: int, c: int) -> float:
+        return self.lib.orc_normal_f64(seed & 0xFFFFFFFF, c & 0xFFFFFFFF)
+
+    def zexp(self, t: float) -> float:
+        return self.lib.orc_zexp(t)
+
+    def zlog(self, x: float) -> float:
+        return self.lib.orc_zlog(x)
+
+    def zig_table(self, N: int):
+        """(X, F, r, v) for an N-layer ziggurat; X and F have N+1 entries."""
+        X = np.empty(N + 1, np.float64)
+        F = np.empty(N + 1, np.float64)
+        r, v = C.c_double(), C.c_double()
+        if self.lib.orc_zig_table(N, _ptr(X), _ptr(F), C.byref(r), C.byref(v)) != 0:
+            raise ValueError("N must be at least 2")
+        return X, F, r.value, v.value
+
+    def zig1024(self):
+        X = np.empty(1025, np.float64)
+        F = np.empty(1025, np.float64)
+        self.lib.orc_zig1024(_ptr(X), _ptr(F))
+        return X, F
+
+    # Fills (element i at counter first + i, or first + idx[i]) ---------------
+    def _fill(self, fn, dtype, seed, first, n, idx, *extra):
+        n, idx = _idx(n, idx)
+        out = np.empty(n, dtype)
+        getattr(self.lib, fn)(seed & 0xFFFFFFFF, first & 0xFFFFFFFF, n, _ptr(idx),
+                              *extra, _ptr(out))
+        return out
+
+    def fill_u32(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_u32", np.uint32, seed, first, n, idx)
+
+    def fill_u64(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_u64", np.uint64, seed, first, n, idx)
+
+    def fill_f32(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_f32", np.float32, seed, first, n, idx)
+
+    def fill_f64(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_f64", np.float64, seed, first, n, idx)
+
+    def fill_u32_below(self, seed, first, bound, n=None, idx=None):
+        return self._fill("orc_fill_u32_below", np.uint32, seed, first, n, idx, bound)
+
+    def fill_u64_below(self, seed, first, bound, n=None, idx=None):
+        return self._fill("orc_fill_u64_below", np.uint64, seed, first, n, idx, bound)
+
+    def fill_i32_range(self, seed, first, low, bound, n=None, idx=None):
+        return self._fill("orc_fill_i32_range", np.int32, seed, first, n, idx, low, bound)
+
+    def fill_i64_range32(self, seed, first, low, bound, n=None, idx=None):
+        return self._fill("orc_fill_i64_range32", np.int64, seed, first, n, idx, low, bound)
+
+    def fill_i64_range(self, seed, first, low, bound, n=None, idx=None):
+        return self._fill("orc_fill_i64_range", np.int64, seed, first, n, idx, low, bound)
+
+    def fill_randn(self, seed, first, n=None, idx=None):
+        """binary64 values of the randn definition (not rounded to f32)."""
+        return self._fill("orc_fill_randn", np.float64, seed, first, n, idx)
+
+    def fill_normal_f64(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_normal_f64", np.float64, seed, first, n, idx)
+
+    def fill_zig_fast(self, seed, first, n=None, idx=None):
+        """1 where the element's first draw takes the ziggurat's fast path."""
+        return self._fill("orc_fill_zig_fast", np.uint8, seed, first, n, idx)
+
+    def dropout(self, x, p, seed, first, idx=None):
+        """dropout of f32 x, x[i] at counter first + i (or first + idx[i])."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        n, idx = _idx(x.size, idx)
+        if n != x.size:
+            raise ValueError("x and idx differ in length")
+        out = np.empty(n, np.float32)
+        self.lib.orc_dropout_fill(_ptr(x), float(np.float32(p)), seed & 0xFFFFFFFF,
+                                  first & 0xFFFFFFFF, n, _ptr(idx), _ptr(out))
+        return out
+
+    def zexp_array(self, t):
+        t = np.ascontiguousarray(t, dtype=np.float64)
+        out = np.empty_like(t)
+        self.lib.orc_zexp_fill(_ptr(t), t.size, _ptr(out))
+        return out
+
+    def zlog_array(self, x):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty_like(x)
+        self.lib.orc_zlog_fill(_ptr(x), x.size, _ptr(out))
+        return out
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    """The oracle built from oracle.c (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def variant(source_text: str, out_dir: str) -> Oracle:
+    return Oracle(compile_variant(source_text, out_dir))
+
+
+def __getattr__(name):
+    # oracle.fill_u32(...) etc. forward to the default instance.
+    if not name.startswith("_") and hasattr(Oracle, name):
+        return getattr(default(), name)
+    raise AttributeError(name)

@@ -1,0 +1,537 @@
+/*
+ * oracle.c -- plain, slow, single-threaded CPU oracle for the stateless
+ * counter-based lowbias32 random fills.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file: only the tests, the package smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or constant with
+ * the CUDA path; both are written independently from the definitions below.
+ *
+ * Every function is written as the plain definition, one element at a time,
+ * in the order the sources state it.  Citations name the web page and the
+ * section the definition comes from:
+ *   [Phobos]  Phobos stdlib, "Random numbers" (sections hash32, uniform,
+ *             randn, dropout; source std/random.ph).
+ *   [Tandem-D] tandem-sycl, "Design" (sections Fills, Normals).
+ *   [Tandem-P] tandem-cuda, "Performance" (section GPU, bounded fills).
+ *   [PK]      perturbation-kernel, "Backends" (section "Why the GPU can be
+ *             exact": Lemire's multiply-shift with rejection).
+ * Readings the pages leave open are marked READING and are listed in the
+ * design notes of the repository.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fexcess-precision=standard
+ *        -fPIC -shared oracle.c -o liboracle.so -lm [-lquadmath on x86-64]
+ * (no contraction of a*b+c into fma: every rounding below is the one written).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#if defined(__aarch64__)
+/* long double is IEEE binary128 on aarch64 Linux. */
+typedef long double quad;
+#define Q_EXP expl
+#define Q_LOG logl
+#define Q_SQRT sqrtl
+#define Q_ERFC erfcl
+#define Q_ACOS acosl
+#elif defined(__x86_64__)
+#include <quadmath.h>
+typedef __float128 quad;
+#define Q_EXP expq
+#define Q_LOG logq
+#define Q_SQRT sqrtq
+#define Q_ERFC erfcq
+#define Q_ACOS acosq
+#else
+#error "the oracle needs a binary128 type (aarch64 long double or x86-64 __float128)"
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* hash32 = lowbias32 [Phobos, section hash32, std/random.ph:13]             */
+/* ------------------------------------------------------------------------ */
+
+/* _mix(x, s) = x ^ (x >>> s).  The page states the shifts are logical: an
+ * arithmetic >> on the signed i32 has the bits it copies in masked off, which
+ * is a logical shift of the 32-bit pattern.  READING: the body of _mix is not
+ * printed; an xorshift by s is the reading the tile mean pins. */
+static uint32_t mix(uint32_t x, unsigned s) { return x ^ (x >> s); }
+
+/* Wrapping 32-bit multiplies by 2146121005 = 0x7FEB352D and by
+ * -2073254261, whose two's-complement pattern is 0x846CA68B. */
+uint32_t orc_hash32(uint32_t x)
+{
+    x = mix(x, 16);
+    x = x * 2146121005u;
+    x = mix(x, 15);
+    x = x * (uint32_t)(-2073254261);
+    x = mix(x, 16);
+    return x;
+}
+
+/* The draw behind uniform(seed, counter): hash32(counter ^ hash32(seed))
+ * [Phobos, section uniform, std/random.ph:21]. */
+uint32_t orc_draw32(uint32_t seed, uint32_t counter)
+{
+    return orc_hash32(counter ^ orc_hash32(seed));
+}
+
+/* 64-bit draw: the 32-bit draw at counter 2c is the high word and the one at
+ * 2c+1 the low word, counters wrapping mod 2^32 (as randn consumes 2c and
+ * 2c+1 [Phobos, section randn]). */
+uint64_t orc_draw64(uint32_t seed, uint32_t counter)
+{
+    uint32_t c2 = 2u * counter;
+    return ((uint64_t)orc_draw32(seed, c2) << 32) | (uint64_t)orc_draw32(seed, c2 + 1u);
+}
+
+/* uniform(seed, c) = f32(draw & 8388607) * 1.1920928955078125e-7, the low 23
+ * bits on a 2^-23 grid in [0, 1) [Phobos, section uniform].  The literal is
+ * exactly 2^-23 and the product is exact. */
+float orc_uniform_f32(uint32_t seed, uint32_t counter)
+{
+    return (float)(orc_draw32(seed, counter) & 8388607u) * 1.1920928955078125e-7f;
+}
+
+/* f64 uniform: the top 53 bits of the 64-bit draw times 2^-53 (exact). */
+double orc_uniform_f64(uint32_t seed, uint32_t counter)
+{
+    return (double)(orc_draw64(seed, counter) >> 11) * 0x1p-53;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Substreams for retries and ziggurat misses [Tandem-D, section Normals:     */
+/* a draw that misses continues on split(g) of sub(PURPOSE) of the key, g the */
+/* draw's global index].  READING, restated in hash32: the purpose key is     */
+/* hash32(hash32(seed) ^ P), the element key hash32(g ^ purpose key) with g   */
+/* the element's own counter, and the k-th word hash32(k ^ element key).      */
+/* ------------------------------------------------------------------------ */
+
+#define PURPOSE_BELOW32 0x42333220u  /* "B32 " */
+#define PURPOSE_BELOW64 0x42363420u  /* "B64 " */
+#define PURPOSE_NORMAL64 0x4E363420u /* "N64 " */
+
+static uint32_t substream_key(uint32_t seed, uint32_t purpose, uint32_t g)
+{
+    uint32_t purpose_key = orc_hash32(orc_hash32(seed) ^ purpose);
+    return orc_hash32(g ^ purpose_key);
+}
+
+static uint32_t substream32(uint32_t key, uint32_t k) { return orc_hash32(k ^ key); }
+
+static uint64_t substream64(uint32_t key, uint32_t k)
+{
+    return ((uint64_t)substream32(key, 2u * k) << 32) | (uint64_t)substream32(key, 2u * k + 1u);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Bounded integers: Lemire's multiply-shift with rejection [PK; Tandem-P].  */
+/* ------------------------------------------------------------------------ */
+
+/* One step on a w-bit word x (1 <= w <= 64) for the bound b (1 <= b < 2^w):
+ * the 2w-bit product x*b; its high w bits are the candidate value and it is
+ * accepted when its low w bits are at least 2^w mod b (Lemire 2019, "Fast
+ * Random Integer Generation in an Interval", exact threshold).  READING: the
+ * exact threshold, not the conservative zone of the perturbation-kernel page;
+ * both are exactly uniform. */
+int orc_lemire_step(uint64_t x, uint64_t b, unsigned w, uint64_t *value)
+{
+    unsigned __int128 two_w = (unsigned __int128)1 << w;
+    unsigned __int128 prod = (unsigned __int128)x * b;
+    uint64_t low = (uint64_t)(prod % two_w);
+    uint64_t threshold = (uint64_t)(two_w % b);
+    *value = (uint64_t)(prod / two_w);
+    return low >= threshold;
+}
+
+/* below32(b): the element's 32-bit draw, then the B32 substream's words. */
+uint32_t orc_below32(uint32_t seed, uint32_t counter, uint32_t b)
+{
+    uint64_t v;
+    if (b == 0) return 0; /* rejected by the API; never sampled */
+    if (orc_lemire_step(orc_draw32(seed, counter), b, 32, &v)) return (uint32_t)v;
+    uint32_t key = substream_key(seed, PURPOSE_BELOW32, counter);
+    for (uint32_t k = 0;; ++k)
+        if (orc_lemire_step(substream32(key, k), b, 32, &v)) return (uint32_t)v;
+}
+
+/* below64(b): the element's 64-bit draw, then the B64 substream's words. */
+uint64_t orc_below64(uint32_t seed, uint32_t counter, uint64_t b)
+{
+    uint64_t v;
+    if (b == 0) return 0;
+    if (orc_lemire_step(orc_draw64(seed, counter), b, 64, &v)) return v;
+    uint32_t key = substream_key(seed, PURPOSE_BELOW64, counter);
+    for (uint32_t k = 0;; ++k)
+        if (orc_lemire_step(substream64(key, k), b, 64, &v)) return v;
+}
+
+/* low + below(b), wrapped to the output type (two's complement)
+ * [Tandem-P, rows "with a low bound into int32_t / int64_t"]. */
+int32_t orc_range_i32(uint32_t seed, uint32_t counter, int32_t low, uint32_t b)
+{
+    return (int32_t)((uint32_t)low + orc_below32(seed, counter, b));
+}
+
+int64_t orc_range_i64_32(uint32_t seed, uint32_t counter, int64_t low, uint32_t b)
+{
+    return (int64_t)((uint64_t)low + (uint64_t)orc_below32(seed, counter, b));
+}
+
+int64_t orc_range_i64(uint32_t seed, uint32_t counter, int64_t low, uint64_t b)
+{
+    return (int64_t)((uint64_t)low + orc_below64(seed, counter, b));
+}
+
+/* ------------------------------------------------------------------------ */
+/* randn [Phobos, section randn, std/random.ph:26]                           */
+/* ------------------------------------------------------------------------ */
+
+/* sqrt(-2 log(1 - uniform(seed, 2c))) * cos(6.283185307179586 uniform(seed,
+ * 2c+1)), evaluated in binary64 from the two f32 uniforms and returned
+ * unrounded to f32 (the reference value the f32 path is held to). */
+double orc_randn(uint32_t seed, uint32_t counter)
+{
+    double u0 = (double)orc_uniform_f32(seed, 2u * counter);
+    double u1 = (double)orc_uniform_f32(seed, 2u * counter + 1u);
+    return sqrt(-2.0 * log(1.0 - u0)) * cos(6.283185307179586 * u1);
+}
+
+/* ------------------------------------------------------------------------ */
+/* dropout [Phobos, section dropout, std/random.ph:30]                       */
+/* ------------------------------------------------------------------------ */
+
+/* where(uniform(seed, c) >= p, x / (1 - p), 0), all in f32 with IEEE
+ * division; a tie u == p is kept. */
+float orc_dropout(float x, float p, uint32_t seed, uint32_t counter)
+{
+    float u = orc_uniform_f32(seed, counter);
+    float keep_scale_divisor = 1.0f - p;
+    return (u >= p) ? x / keep_scale_divisor : 0.0f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Deterministic binary64 exp and log for the ziggurat's slow path.          */
+/* Both are fixed sequences of IEEE operations (+, -, *, /, fma, rint), so a */
+/* second implementation that performs the same operations in the same order */
+/* returns the same bits on any IEEE machine.                                */
+/* ------------------------------------------------------------------------ */
+
+/* ln 2 split for Cody & Waite's argument reduction (Cody & Waite 1980,
+ * "Software Manual for the Elementary Functions"): the high part is ln 2
+ * rounded to 32 significant bits, so k * high is exact for |k| < 2^21; the
+ * low part is ln 2 - high rounded to binary64. */
+static const double LN2_HIGH = 0x1.62e42ffp-1;
+static const double LN2_LOW = -0x1.718432a1b0e26p-35;
+static const double INV_LN2 = 0x1.71547652b82fep+0; /* 1/ln 2 rounded */
+static const double SQRT2 = 0x1.6a09e667f3bcdp+0;   /* sqrt 2 rounded */
+
+/* exp(t): k = rint(t / ln 2), r = t - k ln 2 by two fma, then the Taylor
+ * polynomial of degree 13 in Horner form, then the exact scaling by 2^k.
+ * Valid where the result is a normal number (the slow path needs t in
+ * [-10, 0]). */
+double orc_zexp(double t)
+{
+    double k = rint(t * INV_LN2);
+    double r = fma(-k, LN2_HIGH, t);
+    r = fma(-k, LN2_LOW, r);
+    double p = 1.0 / 6227020800.0; /* 1/13! */
+    p = fma(p, r, 1.0 / 479001600.0); /* 1/12! */
+    p = fma(p, r, 1.0 / 39916800.0);  /* 1/11! */
+    p = fma(p, r, 1.0 / 3628800.0);   /* 1/10! */
+    p = fma(p, r, 1.0 / 362880.0);    /* 1/9! */
+    p = fma(p, r, 1.0 / 40320.0);     /* 1/8! */
+    p = fma(p, r, 1.0 / 5040.0);      /* 1/7! */
+    p = fma(p, r, 1.0 / 720.0);       /* 1/6! */
+    p = fma(p, r, 1.0 / 120.0);       /* 1/5! */
+    p = fma(p, r, 1.0 / 24.0);        /* 1/4! */
+    p = fma(p, r, 1.0 / 6.0);         /* 1/3! */
+    p = fma(p, r, 0.5);               /* 1/2! */
+    p = fma(p, r, 1.0);               /* 1/1! */
+    p = fma(p, r, 1.0);               /* 1/0! */
+    return ldexp(p, (int)k);
+}
+
+/* log(x) for normal positive x: x = 2^e m with m in (sqrt(1/2), sqrt 2],
+ * s = (m - 1)/(m + 1), log m = 2 atanh s = 2 (s + s^3/3 + ... + s^23/23)
+ * (Abramowitz & Stegun 4.1.27), then log x = e ln 2 + log m with the split
+ * ln 2 above. */
+double orc_zlog(double x)
+{
+    uint64_t bits;
+    memcpy(&bits, &x, sizeof bits);
+    int e = (int)(bits >> 52) - 1023;
+    uint64_t mbits = (bits & 0x000FFFFFFFFFFFFFull) | 0x3FF0000000000000ull;
+    double m;
+    memcpy(&m, &mbits, sizeof m);
+    if (m > SQRT2) {
+        m = m * 0.5;
+        e = e + 1;
+    }
+    double s = (m - 1.0) / (m + 1.0);
+    double s2 = s * s;
+    double p = 1.0 / 23.0;
+    p = fma(p, s2, 1.0 / 21.0);
+    p = fma(p, s2, 1.0 / 19.0);
+    p = fma(p, s2, 1.0 / 17.0);
+    p = fma(p, s2, 1.0 / 15.0);
+    p = fma(p, s2, 1.0 / 13.0);
+    p = fma(p, s2, 1.0 / 11.0);
+    p = fma(p, s2, 1.0 / 9.0);
+    p = fma(p, s2, 1.0 / 7.0);
+    p = fma(p, s2, 1.0 / 5.0);
+    p = fma(p, s2, 1.0 / 3.0);
+    double two_s = s + s;
+    double log_m = fma(two_s * s2, p, two_s);
+    double de = (double)e;
+    return fma(de, LN2_HIGH, fma(de, LN2_LOW, log_m));
+}
+
+/* ------------------------------------------------------------------------ */
+/* 1024-layer Marsaglia-Tsang ziggurat [Tandem-D, section Normals]           */
+/* (Marsaglia & Tsang 2000, "The Ziggurat Method for Generating Random       */
+/* Variables").                                                              */
+/* ------------------------------------------------------------------------ */
+
+#define ZIG_LAYERS 1024
+
+static quad qf(quad x) { return Q_EXP(-x * x / 2); }
+
+/* Tail area plus base rectangle for the rightmost edge r:
+ * v = r f(r) + integral_r^inf f = r f(r) + sqrt(pi/2) erfc(r / sqrt 2). */
+static quad zig_area(quad r)
+{
+    quad pi = Q_ACOS((quad)-1);
+    return r * qf(r) + Q_SQRT(pi / 2) * Q_ERFC(r / Q_SQRT((quad)2));
+}
+
+/* Residual of the top layer for a trial r: build X[1] = r, X[j+1] =
+ * f^-1(f(X[j]) + v/X[j]) up to X[N-1] and return f(X[N-1]) + v/X[N-1] - 1,
+ * which is zero when the top layer (up to f(0) = 1) also has area v.  A layer
+ * that would already pass f(0) means r is too small: return +1. */
+static quad zig_residual(quad r, unsigned N)
+{
+    quad v = zig_area(r);
+    quad x = r;
+    for (unsigned j = 1; j + 1 < N; ++j) {
+        quad y = qf(x) + v / x;
+        if (y >= 1) return 1;
+        x = Q_SQRT(-2 * Q_LOG(y));
+    }
+    return qf(x) + v / x - 1;
+}
+
+/* Table for N layers, each entry the binary128 value rounded once to binary64:
+ * r the root of the residual (bisection to binary128 resolution), X[0] =
+ * v/f(r), X[1] = r, X[j+1] as above, X[N] = 0, F[j] = f(X[j]), F[N] = 1.
+ * X and F hold N+1 entries.  Returns 0, or -1 for N < 2. */
+int orc_zig_table(unsigned N, double *X, double *F, double *r_out, double *v_out)
+{
+    if (N < 2) return -1;
+    quad lo = 1, hi = 10;
+    for (int it = 0; it < 200; ++it) {
+        quad mid = (lo + hi) / 2;
+        if (mid == lo || mid == hi) break;
+        if (zig_residual(mid, N) > 0)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    quad r = (lo + hi) / 2;
+    quad v = zig_area(r);
+    quad x = r;
+    X[0] = (double)(v / qf(r));
+    F[0] = (double)qf(v / qf(r));
+    X[1] = (double)r;
+    F[1] = (double)qf(r);
+    for (unsigned j = 1; j + 1 < N; ++j) {
+        x = Q_SQRT(-2 * Q_LOG(qf(x) + v / x));
+        X[j + 1] = (double)x;
+        F[j + 1] = (double)qf(x);
+    }
+    X[N] = 0.0;
+    F[N] = 1.0;
+    if (r_out) *r_out = (double)r;
+    if (v_out) *v_out = (double)v;
+    return 0;
+}
+
+static double zig_X[ZIG_LAYERS + 1], zig_F[ZIG_LAYERS + 1];
+static int zig_ready;
+
+static void zig_init(void)
+{
+    if (!zig_ready) {
+        orc_zig_table(ZIG_LAYERS, zig_X, zig_F, NULL, NULL);
+        zig_ready = 1;
+    }
+}
+
+/* Copy of the 1024-layer table the normals use (1025 entries each). */
+void orc_zig1024(double *X, double *F)
+{
+    zig_init();
+    memcpy(X, zig_X, sizeof zig_X);
+    memcpy(F, zig_F, sizeof zig_F);
+}
+
+/* Fast-path test of one 64-bit draw w: layer j = the low 10 bits, sign bit
+ * 10, magnitude x = (w >> 11) 2^-53 X[j] (one rounded multiply); the draw is
+ * taken when x < X[j+1].  READING: this bit layout (10 + 1 + 53 = 64 bits). */
+static int zig_fast(uint64_t w, double *x_out, unsigned *j_out, int *neg_out)
+{
+    unsigned j = (unsigned)(w & (ZIG_LAYERS - 1));
+    int neg = (int)((w >> 10) & 1u);
+    double x = ((double)(w >> 11) * 0x1p-53) * zig_X[j];
+    *x_out = x;
+    *j_out = j;
+    *neg_out = neg;
+    return x < zig_X[j + 1];
+}
+
+/* 1 when the element's first draw takes the fast path, 0 when it misses. */
+int orc_zig_first_draw_fast(uint32_t seed, uint32_t counter)
+{
+    double x;
+    unsigned j;
+    int neg;
+    zig_init();
+    return zig_fast(orc_draw64(seed, counter), &x, &j, &neg);
+}
+
+/* One standard normal per counter.  Element c takes the 64-bit draw at c; a
+ * miss continues on the N64 substream of its own counter: the base layer's
+ * miss samples the tail (Marsaglia 1964: a = -log(U1)/r, b = -log(U2), accept
+ * when 2b >= a^2, value r + a, U in (0, 1]); another layer's miss takes the
+ * wedge test y = F[j] + U (F[j+1] - F[j]) < exp(-x^2/2) and otherwise starts
+ * over with a fresh 64-bit word.  READING: this order of substream words. */
+double orc_normal_f64(uint32_t seed, uint32_t counter)
+{
+    zig_init();
+    uint64_t w = orc_draw64(seed, counter);
+    uint32_t key = substream_key(seed, PURPOSE_NORMAL64, counter);
+    uint32_t k = 0;
+    for (;;) {
+        double x;
+        unsigned j;
+        int neg;
+        if (zig_fast(w, &x, &j, &neg)) return neg ? -x : x;
+        if (j == 0) {
+            double r = zig_X[1];
+            for (;;) {
+                double u1 = (double)((substream64(key, k) >> 11) + 1) * 0x1p-53;
+                double u2 = (double)((substream64(key, k + 1u) >> 11) + 1) * 0x1p-53;
+                k += 2u;
+                double a = -orc_zlog(u1) / r;
+                double b = -orc_zlog(u2);
+                if (b + b >= a * a) {
+                    double z = r + a;
+                    return neg ? -z : z;
+                }
+            }
+        }
+        double u = (double)(substream64(key, k) >> 11) * 0x1p-53;
+        k += 1u;
+        double y = zig_F[j] + u * (zig_F[j + 1] - zig_F[j]);
+        double t = x * x;
+        t = t * -0.5;
+        if (y < orc_zexp(t)) return neg ? -x : x;
+        w = substream64(key, k);
+        k += 1u;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fills.  Element i of a fill takes the counter first + i mod 2^32; with a  */
+/* non-NULL idx, output slot i holds element idx[i] of the fill instead      */
+/* (sampled checks of large fills).                                          */
+/* ------------------------------------------------------------------------ */
+
+static uint32_t counter_of(uint32_t first, const uint64_t *idx, size_t i)
+{
+    return first + (uint32_t)(idx ? idx[i] : (uint64_t)i);
+}
+
+void orc_fill_u32(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint32_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_draw32(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_u64(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint64_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_draw64(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_f32(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, float *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_uniform_f32(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_f64(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_uniform_f64(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_u32_below(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint32_t b,
+                        uint32_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_below32(seed, counter_of(first, idx, i), b);
+}
+
+void orc_fill_u64_below(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint64_t b,
+                        uint64_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_below64(seed, counter_of(first, idx, i), b);
+}
+
+void orc_fill_i32_range(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, int32_t low,
+                        uint32_t b, int32_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_range_i32(seed, counter_of(first, idx, i), low, b);
+}
+
+void orc_fill_i64_range32(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, int64_t low,
+                          uint32_t b, int64_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_range_i64_32(seed, counter_of(first, idx, i), low, b);
+}
+
+void orc_fill_i64_range(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, int64_t low,
+                        uint64_t b, int64_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_range_i64(seed, counter_of(first, idx, i), low, b);
+}
+
+void orc_fill_randn(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_randn(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_normal_f64(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_normal_f64(seed, counter_of(first, idx, i));
+}
+
+/* x[i] is the input of output slot i (element idx[i] when idx is given). */
+void orc_dropout_fill(const float *x, float p, uint32_t seed, uint32_t first, size_t n,
+                      const uint64_t *idx, float *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_dropout(x[i], p, seed, counter_of(first, idx, i));
+}
+
+/* out[i] = 1 when the first draw of element i takes the ziggurat's fast path. */
+void orc_fill_zig_fast(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint8_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = (uint8_t)orc_zig_first_draw_fast(seed, counter_of(first, idx, i));
+}
+
+void orc_zexp_fill(const double *t, size_t n, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_zexp(t[i]);
+}
+
+void orc_zlog_fill(const double *x, size_t n, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_zlog(x[i]);
+}

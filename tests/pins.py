@@ -1,0 +1,431 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each pin takes an ``oracle.Oracle`` and raises AssertionError when the facts
+do not hold.  ``test_oracle_pins.py`` runs every pin on the oracle;
+``test_oracle_mutations.py`` plants plausible mistakes in copies of the
+oracle and checks that a pin fails on each.  The facts come from the pages
+(worked examples under tests/golden/, each cited there), from closed forms and
+from exhaustive or brute-force enumeration on small cases.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy import special, stats
+
+from helpers import golden
+
+U32 = 1 << 32
+U64 = 1 << 64
+
+
+def _ulps(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    return np.abs(a - b) / np.spacing(np.maximum(np.abs(a), np.abs(b)))
+
+
+# ---------------------------------------------------------------- hash32 ---
+def pin_tile_mean(orc):
+    """Phobos 'Random numbers' tile figure: seed 1, counters (r + iota(0)) * 32
+    + iota(1) over an 8 x 32 tile, mean 0.513, every value k * 2^-23 in [0, 1)."""
+    g = golden("phobos_uniform_tile.txt")
+    rows, cols, seed = int(g["rows"]), int(g["cols"]), int(g["seed"])
+    c = (np.arange(rows)[:, None] * cols + np.arange(cols)[None, :]).ravel()
+    u = orc.fill_f32(seed, 0, idx=c).astype(np.float64)
+    assert round(float(u.mean()), 3) == float(g["mean_3dp"]), u.mean()
+    scaled = u * 2.0 ** -int(g["grid_log2"])
+    assert np.all(scaled == np.floor(scaled)) and np.all((u >= 0) & (u < 1))
+
+
+def pin_uniform_grid(orc):
+    """Every uniform is a multiple of 2^-23 in [0, 1); 2^24 consecutive counters
+    give 2^24 distinct draws (a bijection of the counter), and the uniform is
+    the draw's low 23 bits.  (No chi-square here: hash32 of consecutive
+    counters has a small but detectable bias in 1024-bin histograms at 2^24
+    draws, a property of the method itself.)"""
+    seed = 0x9E3779B9
+    u = orc.fill_f32(seed, 0, 1 << 24).astype(np.float64)
+    k = u * 2.0 ** 23
+    assert np.all(k == np.floor(k)) and k.min() >= 0 and k.max() < 2 ** 23
+    d = orc.fill_u32(seed, 0, 1 << 24)
+    assert np.array_equal(d & 0x7FFFFF, k.astype(np.uint32))
+    d.sort()
+    assert np.all(np.diff(d) != 0)
+
+
+def pin_hash_bijective(orc):
+    """lowbias32 is a bijection of the 32-bit words (odd multipliers and
+    xorshifts are invertible): undo each step with its inverse and recover the
+    counter; the seed enters only as the XOR key hash32(seed)."""
+    rng = np.random.default_rng(5)
+    c = rng.integers(0, U32, 1 << 18, dtype=np.uint64)
+    seed = 0x12345678
+    y = orc.fill_u32(seed, 0, idx=c).astype(np.uint64)
+    m1, m2 = 2146121005, (-2073254261) % U32
+    inv1, inv2 = pow(m1, -1, U32), pow(m2, -1, U32)
+    x = y ^ (y >> 16)
+    x = (x * inv2) & 0xFFFFFFFF
+    x = x ^ (x >> 15) ^ (x >> 30)
+    x = (x * inv1) & 0xFFFFFFFF
+    x = x ^ (x >> 16)
+    assert np.array_equal(x ^ orc.hash32(seed), c)
+
+
+# --------------------------------------------------------- 64-bit draws ----
+def pin_draw64_words(orc):
+    """The 64-bit draw holds the 32-bit draw at 2c in its high word and the one
+    at 2c + 1 in its low word, 2c wrapping mod 2^32; the f64 uniform is its top
+    53 bits times 2^-53, exactly."""
+    seed = 0x9E3779B9
+    c = np.array([0, 1, 3, (1 << 31) - 1, 1 << 31, (1 << 31) + 5, U32 - 5, U32 - 1], np.uint64)
+    d64 = orc.fill_u64(seed, 0, idx=c)
+    hi = orc.fill_u32(seed, 0, idx=(2 * c) % U32).astype(np.uint64)
+    lo = orc.fill_u32(seed, 0, idx=(2 * c + 1) % U32).astype(np.uint64)
+    assert np.array_equal(d64, (hi << np.uint64(32)) | lo)
+    f = orc.fill_f64(seed, 0, idx=c)
+    assert np.array_equal(f * 2.0 ** 53, (d64 >> np.uint64(11)).astype(np.float64))
+    assert np.all((f >= 0) & (f < 1))
+
+
+# ------------------------------------------------------- bounded integers --
+def pin_lemire_exhaustive_8bit(orc):
+    """Over every 8-bit word and every bound 1..255, the multiply-shift with
+    its rejection threshold gives each value in [0, b) exactly floor(256/b)
+    times and rejects exactly 256 mod b words: the same histogram as brute-force
+    rejection (accept x < b * floor(256/b), return x mod b)."""
+    w = 8
+    for b in range(1, 256):
+        hist = np.zeros(b, np.int64)
+        rejected = 0
+        for x in range(1 << w):
+            ok, v = orc.lemire_step(x, b, w)
+            if ok:
+                assert v < b
+                hist[v] += 1
+            else:
+                rejected += 1
+        brute = np.bincount([x % b for x in range(1 << w) if x < b * ((1 << w) // b)], minlength=b)
+        assert np.array_equal(hist, brute), b
+        assert rejected == (1 << w) % b, b
+
+
+def pin_lemire_exhaustive_16bit(orc):
+    """As above on 16-bit words for bounds that cover tiny, odd, power-of-two
+    and near-maximal ranges."""
+    w = 16
+    for b in (1, 3, 7, 1000, 4096, 32769, 65535):
+        hist = np.zeros(b, np.int64)
+        rejected = 0
+        for x in range(1 << w):
+            ok, v = orc.lemire_step(x, b, w)
+            if ok:
+                hist[v] += 1
+            else:
+                rejected += 1
+        assert hist.min() == hist.max() == (1 << w) // b, b
+        assert rejected == (1 << w) % b, b
+
+
+def pin_lemire_wide_words(orc):
+    """On 32- and 64-bit words the step is floor(x b / 2^w), accepted iff
+    (x b) mod 2^w >= 2^w mod b, evaluated here with exact Python integers."""
+    rng = np.random.default_rng(9)
+    for w in (32, 64):
+        for _ in range(2000):
+            x = int(rng.integers(0, 1 << 62)) * 4 + int(rng.integers(0, 4))
+            x %= 1 << w
+            b = int(rng.integers(1, 1 << 62)) % (1 << w) or 1
+            ok, v = orc.lemire_step(x, b, w)
+            assert v == (x * b) >> w
+            assert ok == (((x * b) % (1 << w)) >= ((1 << w) % b))
+
+
+def _chi2_uniform(values: np.ndarray, b: int, bins: int = 64) -> float:
+    idx = (values.astype(object) * bins // b).astype(np.int64) if b >= U32 else (
+        values.astype(np.uint64) * np.uint64(bins) // np.uint64(b)).astype(np.int64)
+    obs = np.bincount(idx, minlength=bins).astype(np.float64)
+    lo = np.array([(k * b + bins - 1) // bins for k in range(bins + 1)], dtype=object)
+    exp = np.array([float(lo[k + 1] - lo[k]) / b for k in range(bins)]) * values.size
+    return stats.chisquare(obs, exp).pvalue
+
+
+def pin_below_distributions(orc):
+    """below32 / below64 values lie in [0, b) and are uniform, including bounds
+    where about half of all words are rejected (b = 2^31 + 1, 2^63 + 1), so the
+    substream retries carry half of the values."""
+    n = 1 << 17
+    for b in (1000, (1 << 31) + 1, U32 - 2):
+        v = orc.fill_u32_below(1, 0, b, n)
+        assert int(v.max()) < b
+        assert _chi2_uniform(v, b) > 1e-4, b
+    for b in (1000, (1 << 63) + 1, U64 - 2):
+        v = orc.fill_u64_below(2, 0, b, n)
+        assert int(v.max()) < b
+        if b < U32:
+            assert _chi2_uniform(v, b) > 1e-4, b
+        else:
+            hi = (v.astype(object) * 64 // b).astype(np.int64)
+            assert stats.chisquare(np.bincount(hi, minlength=64)).pvalue > 1e-4, b
+    assert not np.any(orc.fill_u32_below(3, 0, 1, 4096))
+    # First words rejected at about (2^31 - 1) / 2^32 for b = 2^31 + 1
+    b = (1 << 31) + 1
+    d = orc.fill_u32(4, 0, 1 << 15)
+    rejected = sum(not orc.lemire_step(int(x), b, 32)[0] for x in d)
+    p = ((1 << 31) - 1) / U32
+    assert abs(rejected / d.size - p) < 5 * math.sqrt(p * (1 - p) / d.size)
+
+
+def pin_ranges_wrap(orc):
+    """low + below(b) wraps in two's complement into int32 / int64."""
+    n = 4096
+    low32 = (1 << 31) - 10
+    base = orc.fill_u32_below(3, 7, 1000, n).astype(np.int64)
+    r32 = orc.fill_i32_range(3, 7, low32, 1000, n).astype(np.int64)
+    assert np.array_equal(r32, (low32 + base + (1 << 31)) % U32 - (1 << 31))
+    assert np.array_equal(orc.fill_i64_range32(3, 7, -500, 1000, n), base - 500)
+    b64 = orc.fill_u64_below(3, 7, 1000, n).astype(np.int64)
+    assert np.array_equal(orc.fill_i64_range(3, 7, -500, 1000, n), b64 - 500)
+
+
+# ------------------------------------------------------------------ randn --
+def _counters_with_low23(orc, seed: int, word: int, targets, first_n: int = 1 << 26):
+    """Counters c (< first_n / 2) whose uniform at 2c + word has the given 23-bit grid index."""
+    d = orc.fill_u32(seed, word, first_n)[::2] & 0x7FFFFF
+    return {t: np.nonzero(d == t)[0] for t in targets}
+
+
+def pin_randn_special_angles(orc):
+    """Closed forms of the Box-Muller value at the angles where cos is exact:
+    u1 = 0 gives +r, u1 = 1/2 gives -r, u1 = 1/4 and 3/4 give |z| < 1e-15 r,
+    with r = sqrt(-2 ln(1 - u0)); u0 = 0 gives z = 0."""
+    seed = 7
+    hits = _counters_with_low23(orc, seed, 1, (0, 1 << 21, 1 << 22, 3 << 21))
+    for t, cs in hits.items():
+        assert cs.size, t
+        u0 = orc.fill_f32(seed, 0, idx=(2 * cs) % U32).astype(np.float64)
+        r = np.sqrt(-2.0 * np.log1p(-u0))
+        z = orc.fill_randn(seed, 0, idx=cs)
+        if t == 0:
+            assert np.allclose(z, r, rtol=1e-15, atol=0)
+        elif t == 1 << 22:
+            assert np.allclose(z, -r, rtol=1e-15, atol=0)
+        else:
+            assert np.all(np.abs(z) <= 1e-15 * r + 1e-300)
+    zero = _counters_with_low23(orc, seed, 0, (0,))[0]
+    assert zero.size and np.all(orc.fill_randn(seed, 0, idx=zero) == 0)
+
+
+def pin_randn_tail_end(orc):
+    """Phobos 'Random numbers', randn: the 2^-23 grid ends the tails near 5.6,
+    i.e. |z| <= sqrt(-2 ln 2^-23); the largest radius is reached at u0 = 1 - 2^-23."""
+    g = golden("phobos_randn_tail.txt")
+    bound = math.sqrt(-2.0 * math.log(2.0 ** int(g["grid_log2"])))
+    assert round(bound, 1) == float(g["tail_end_1dp"])
+    z = orc.fill_randn(11, 0, 1 << 22)
+    assert np.abs(z).max() <= bound * (1 + 1e-15)
+    top = _counters_with_low23(orc, 11, 0, ((1 << 23) - 1,))[(1 << 23) - 1]
+    assert top.size
+    u1 = orc.fill_f32(11, 0, idx=(2 * top + 1) % U32).astype(np.float64)
+    assert np.allclose(orc.fill_randn(11, 0, idx=top), bound * np.cos(2 * np.pi * u1), rtol=1e-13, atol=1e-13)
+
+
+def _normal_stats(z: np.ndarray):
+    n = z.size
+    assert abs(z.mean()) < 5 / math.sqrt(n), z.mean()
+    assert abs(z.var() - 1) < 5 * math.sqrt(2 / n), z.var()
+    assert abs(stats.skew(z)) < 5 * math.sqrt(6 / n)
+    assert abs(stats.kurtosis(z)) < 5 * math.sqrt(24 / n)
+    edges = stats.norm.ppf(np.linspace(0, 1, 201))
+    obs = np.histogram(z, bins=edges)[0]
+    assert stats.chisquare(obs).pvalue > 1e-3
+
+
+def pin_randn_distribution(orc):
+    """Moments and a 200-bin equiprobable chi-square of 2^22 randn values."""
+    _normal_stats(orc.fill_randn(3, 0, 1 << 22))
+
+
+# ---------------------------------------------------------------- dropout --
+def pin_dropout(orc):
+    """Phobos 'Random numbers', dropout: where(uniform >= p, x / (1 - p), 0)
+    in f32.  Checked against numpy's IEEE f32 division and compare: the mask is
+    uniform >= p (a tie is kept), the kept value is x / (1 - p), dropped
+    elements are +0, the backward pass (same seed and counters) drops the same
+    elements, p = 0 returns x, and the kept fraction is 1 - ceil(p 2^23) / 2^23."""
+    rng = np.random.default_rng(1)
+    n = 1 << 20
+    x = rng.uniform(-1, 1, n).astype(np.float32)
+    for p in (0.1, 0.5, 0.0, 0.999):
+        p32 = np.float32(p)
+        y = orc.dropout(x, p32, 42, 5)
+        u = orc.fill_f32(42, 5, n)
+        keep = u >= p32
+        assert np.array_equal(y[keep].view(np.uint32), (x[keep] / (np.float32(1) - p32)).view(np.uint32))
+        assert np.all(y[~keep].view(np.uint32) == 0)
+        dy = rng.standard_normal(n).astype(np.float32)
+        assert np.array_equal(orc.dropout(dy, p32, 42, 5) != 0, keep & (dy != 0))
+        T = math.ceil(float(p32) * 2 ** 23)
+        q = 1 - T / 2 ** 23
+        assert abs(keep.mean() - q) <= 5 * math.sqrt(q * (1 - q) / n) + 1e-12
+    assert np.array_equal(orc.dropout(x, 0.0, 42, 5).view(np.uint32), x.view(np.uint32))
+    # a tie u == p is kept
+    ties = np.nonzero(orc.fill_f32(42, 0, 1 << 25) == np.float32(0.5))[0]
+    assert ties.size
+    ones = np.ones(ties.size, np.float32)
+    assert np.all(orc.dropout(ones, 0.5, 42, 0, idx=ties) == 2.0)
+    # a dropped NaN is +0
+    nan = np.full(n, np.nan, np.float32)
+    y = orc.dropout(nan, 0.5, 42, 5)
+    assert np.all((y.view(np.uint32) == 0) | np.isnan(y))
+
+
+# ------------------------------------------------------------- exp / log ---
+def pin_zexp_zlog(orc):
+    """The slow path's own exp and log lie within 2 ulp of the C library's on
+    dense samples of their domains, and are exact at the anchors."""
+    rng = np.random.default_rng(3)
+    t = np.concatenate([rng.uniform(-10, 0, 1 << 20), -np.linspace(0, 10, 4097)])
+    assert _ulps(orc.zexp_array(t), np.exp(t)).max() <= 2
+    x = np.concatenate([rng.uniform(0, 1, 1 << 20), 2.0 ** -rng.uniform(0, 53, 1 << 18),
+                        1 - rng.integers(1, 1 << 20, 4096) * 2.0 ** -53, [2.0 ** -53, 0.5, 1.0]])
+    x = x[x > 0]
+    ref = np.log(x)
+    got = orc.zlog_array(x)
+    nz = ref != 0
+    assert _ulps(got[nz], ref[nz]).max() <= 2
+    assert orc.zlog(1.0) == 0 and orc.zexp(0.0) == 1.0
+
+
+# --------------------------------------------------------------- ziggurat --
+def pin_zig_table_published(orc):
+    """Marsaglia & Tsang (2000): the 128-layer normal table has r =
+    3.442619855899 and v = 9.91256303526217e-3; the same generator makes the
+    1024-layer table."""
+    g = golden("marsaglia_tsang_n128.txt")
+    X, F, r, v = orc.zig_table(int(g["layers"]))
+    assert abs(r - float(g["r"])) < 1e-11
+    # the printed v agrees with the exact area to 11 significant digits
+    assert abs(v / float(g["v"]) - 1) < 1e-11
+    assert X[1] == r
+
+
+def pin_zig_table_invariants(orc):
+    """1024 layers of equal area v (the base strip's v = X[0] f(r)); X falls to
+    X[1024] = 0, F = exp(-X^2/2) rises to F[1024] = 1."""
+    X, F = orc.zig1024()
+    _, _, r, v = orc.zig_table(1024)
+    assert X[1] == r and X[1024] == 0 and F[1024] == 1
+    assert np.all(np.diff(X) < 0) and np.all(np.diff(F) > 0)
+    assert np.allclose(F, np.exp(-X * X / 2), rtol=1e-14, atol=0)
+    assert abs(X[0] * F[1] / v - 1) < 1e-15
+    area = X[1:1024] * (F[2:] - F[1:1024])
+    assert np.max(np.abs(area / v - 1)) < 1e-12
+    tail = math.sqrt(math.pi / 2) * special.erfc(r / math.sqrt(2))
+    assert abs((r * F[1] + tail) / v - 1) < 1e-14
+
+
+def pin_zig_miss_rate(orc):
+    """tandem-sycl 'Design', Normals: 0.43 % of draws miss the fast path.  The
+    table's miss probability mean(1 - X[j+1]/X[j]) rounds to it, and the
+    measured first-draw miss fraction agrees within 5 sigma."""
+    g = golden("tandem_ziggurat_miss.txt")
+    X, _ = orc.zig1024()
+    assert X.size - 1 == int(g["layers"])
+    p = float(np.mean(1 - X[1:] / X[:-1]))
+    assert round(100 * p, 2) == float(g["miss_percent_2dp"])
+    n = 1 << 22
+    fast = orc.fill_zig_fast(7, 0, n)
+    miss = 1 - fast.mean()
+    assert abs(miss - p) < 5 * math.sqrt(p * (1 - p) / n), (miss, p)
+
+
+def pin_normal_f64_distribution(orc):
+    """Moments, a 200-bin chi-square, the tail count P(|Z| > r) = erfc(r/sqrt 2)
+    and the shape of the tail beyond r (Kolmogorov-Smirnov against the normal
+    conditioned on |Z| > r) for 2^22 ziggurat normals."""
+    n = 1 << 22
+    z = orc.fill_normal_f64(7, 0, n)
+    _normal_stats(z)
+    X, _ = orc.zig1024()
+    r = X[1]
+    p = special.erfc(r / math.sqrt(2))
+    tail = np.abs(z[np.abs(z) > r])
+    assert abs(tail.size - p * n) < 5 * math.sqrt(p * n), tail.size
+    cdf = lambda t: 1 - special.erfc(t / math.sqrt(2)) / special.erfc(r / math.sqrt(2))
+    assert stats.kstest(tail, cdf).pvalue > 1e-3
+    # the misses on their own (wedges and tail) are normal values too
+    fast = orc.fill_zig_fast(7, 0, n).astype(bool)
+    zm = z[~fast]
+    assert zm.size > 10000
+    assert abs(np.mean(zm)) < 5 * np.std(zm) / math.sqrt(zm.size)
+
+
+def pin_zig_wedge_acceptance(orc):
+    """The wedge test accepts a first-draw miss in layer j >= 1 with probability
+    (integral of f over [X[j+1], X[j]] - F[j] (X[j] - X[j+1])) / wedge area, the
+    area under the curve inside the layer's rectangle beyond X[j+1] (computed
+    here with erf).  The measured acceptance over 2^22 elements agrees within
+    5 sigma; fast-path elements return the draw's own magnitude and sign."""
+    n = 1 << 22
+    X, F = orc.zig1024()
+    w = orc.fill_u64(7, 0, n)
+    j = (w & np.uint64(1023)).astype(np.int64)
+    neg = ((w >> np.uint64(10)) & np.uint64(1)).astype(bool)
+    x = ((w >> np.uint64(11)).astype(np.float64) * 2.0 ** -53) * X[j]
+    fast = x < X[j + 1]
+    assert np.array_equal(fast, orc.fill_zig_fast(7, 0, n).astype(bool))
+    z = orc.fill_normal_f64(7, 0, n)
+    assert np.array_equal(np.abs(z[fast]), x[fast])
+    assert np.array_equal(np.signbit(z[fast]), neg[fast])
+    wedge = ~fast & (j >= 1)
+    accepted = (np.abs(z[wedge]) == x[wedge]) & (np.signbit(z[wedge]) == neg[wedge])
+    k = np.arange(1, 1024)
+    a, b = X[k + 1], X[k]
+    integ = math.sqrt(math.pi / 2) * (special.erf(b / math.sqrt(2)) - special.erf(a / math.sqrt(2)))
+    p_acc = (integ - F[k] * (b - a)) / ((b - a) * (F[k + 1] - F[k]))
+    per_layer = np.zeros(1024)
+    per_layer[1:] = p_acc
+    expected = per_layer[j[wedge]].mean()
+    sigma = math.sqrt(expected * (1 - expected) / wedge.sum())
+    assert abs(accepted.mean() - expected) < 5 * sigma, (accepted.mean(), expected)
+
+
+# ---------------------------------------------------------- slice invariant -
+def pin_slice_invariant(orc):
+    """A fill cut at any element equals the whole fill (tandem-sycl 'Design',
+    Normals), for every fill, across the 2^32 counter wrap; a sampled fill
+    (idx) equals the dense one."""
+    rng = np.random.default_rng(2)
+    n = 3000
+    fills = [
+        lambda f, m, idx=None: orc.fill_u32(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_u64(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_f32(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_f64(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_u32_below(9, f, (1 << 31) + 1, m, idx),
+        lambda f, m, idx=None: orc.fill_u64_below(9, f, (1 << 63) + 1, m, idx),
+        lambda f, m, idx=None: orc.fill_i32_range(9, f, -500, 1000, m, idx),
+        lambda f, m, idx=None: orc.fill_i64_range32(9, f, -500, 1000, m, idx),
+        lambda f, m, idx=None: orc.fill_i64_range(9, f, -500, 1000, m, idx),
+        lambda f, m, idx=None: orc.fill_randn(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_normal_f64(9, f, m, idx),
+    ]
+    for first in (0, 1, 3, U32 - 5):
+        for fill in fills:
+            whole = fill(first, n)
+            for _ in range(3):
+                a, b = sorted(rng.integers(0, n, 2))
+                part = fill((first + int(a)) % U32, int(b - a))
+                assert np.array_equal(part.view(np.uint8), whole[a:b].view(np.uint8))
+            sel = rng.integers(0, n, 257)
+            assert np.array_equal(fill(first, None, sel).view(np.uint8), whole[sel].view(np.uint8))
+
+
+ALL_PINS = [
+    pin_tile_mean, pin_uniform_grid, pin_hash_bijective, pin_draw64_words,
+    pin_lemire_exhaustive_8bit, pin_lemire_exhaustive_16bit, pin_lemire_wide_words,
+    pin_below_distributions, pin_ranges_wrap, pin_randn_special_angles,
+    pin_randn_tail_end, pin_randn_distribution, pin_dropout, pin_zexp_zlog,
+    pin_zig_table_published, pin_zig_table_invariants, pin_zig_miss_rate,
+    pin_normal_f64_distribution, pin_zig_wedge_acceptance, pin_slice_invariant,
+]
