@@ -1,0 +1,76 @@
+// fill_kernel.cuh -- the streaming fill kernel shared by every counter fill.
+//
+// Element i of a piece holds gen(first + i).  The output is cut into a head
+// of fewer than 16/sizeof(T) elements up to its first 16-byte boundary, a
+// body of whole 16-byte vectors and a ragged tail.  Each thread of the body
+// computes one vector's elements in registers and writes them with one
+// 16-byte store, so the 32 lanes of a warp write 512 contiguous bytes (four
+// full 128-byte lines) per store instruction whatever the element type and
+// whatever the first counter: with a stateless hash each element's counter
+// costs nothing, only the output address decides alignment.  The grid is a
+// whole number of waves (resident blocks x SMs) striding over the body.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace rngk {
+
+template <class T>
+struct Vec16 {
+    static constexpr uint32_t kPer = 16 / sizeof(T);
+    T v[kPer];
+};
+
+// Streaming store of one 16-byte vector (evict-first: the output is written
+// once and not re-read by this kernel).
+template <class T>
+__device__ __forceinline__ void store16(T *p, const Vec16<T> &x)
+{
+    uint4 u;
+    static_assert(sizeof(u) == sizeof(x), "16-byte vector");
+    memcpy(&u, &x, sizeof(u));
+    __stcs(reinterpret_cast<uint4 *>(p), u);
+}
+
+template <class Gen>
+__global__ void __launch_bounds__(kFillThreads)
+fill_kernel(Gen gen, typename Gen::T *__restrict__ out, uint32_t first, uint32_t head, uint32_t n_vec,
+            uint32_t n)
+{
+    using T = typename Gen::T;
+    constexpr uint32_t kPer = Vec16<T>::kPer;
+    const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t stride = gridDim.x * blockDim.x;
+
+    const uint32_t tail0 = head + n_vec * kPer;
+    if (tid < head) out[tid] = gen(first + tid);
+    if (tid < n - tail0) out[tail0 + tid] = gen(first + tail0 + tid);
+
+    T *body = out + head;
+    const uint32_t c0 = first + head;
+    for (uint32_t v = tid; v < n_vec; v += stride) {
+        Vec16<T> x;
+        const uint32_t c = c0 + v * kPer;
+#pragma unroll
+        for (uint32_t k = 0; k < kPer; ++k) x.v[k] = gen(c + k);
+        store16(body + v * kPer, x);
+    }
+}
+
+// Launch one piece of n elements (n <= kChunk).
+template <class Gen>
+cudaError_t launch_fill(const Gen &gen, typename Gen::T *out, uint32_t first, uint32_t n, cudaStream_t s)
+{
+    using T = typename Gen::T;
+    const uint32_t head = head_elems<T>(out, n);
+    const uint32_t n_vec = (n - head) / Vec16<T>::kPer;
+    fill_kernel<Gen><<<fill_blocks(n_vec), kFillThreads, 0, s>>>(gen, out, first, head, n_vec, n);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace rngk

@@ -1,0 +1,304 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact for every integer, uniform, bounded, dropout and f64-normal fill;
+within |err| <= 4e-6 (1 + |z|) for the f32 Box-Muller normal.  Sizes span
+several tiles and waves of each kernel plus ragged tails; every fill runs at
+the unaligned starts and the counter wrap, with its output at a 16-byte
+boundary and one element past it."""
+import math
+
+import numpy as np
+import pytest
+
+from dropout_lowbias32_hash32_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+U32 = 1 << 32
+FIRSTS = (0, 1, 3, U32 - 5)
+# 3 waves of the u32 fill (152 SMs x 8 blocks x 256 threads x 4 elements) + a ragged tail
+BIG = 3 * 152 * 8 * 256 * 4 + 13
+SMALL = (1, 2, 3, 5, 15, 16, 17, 31, 33, 1000, 4095, 4096, 4097, 65537)
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    assert torch.cuda.is_available(), "these tests need the GB300"
+    return torch
+
+
+@pytest.fixture(scope="module")
+def rng(torch):
+    import dropout_lowbias32_hash32_gb300 as rng
+    return rng
+
+
+def _out(torch, dtype, n, offset):
+    return torch.empty(n + offset, dtype=dtype, device="cuda")[offset:]
+
+
+def _bits(a: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(a).view(np.uint8)
+
+
+def _host(t):
+    return t.cpu().numpy()
+
+
+def _assert_equal(name, got, want, any_nan=False):
+    if any_nan:
+        # IEEE 754 leaves the payload of a NaN result open: compare NaN-ness
+        # there and bits everywhere else
+        nan_g, nan_w = np.isnan(got), np.isnan(want)
+        assert np.array_equal(nan_g, nan_w), f"{name}: NaN positions differ"
+        got, want = got[~nan_g], want[~nan_w]
+    if not np.array_equal(_bits(got), _bits(want)):
+        g, w = got.view(np.uint8).reshape(got.size, -1), want.view(np.uint8).reshape(want.size, -1)
+        bad = np.nonzero(np.any(g != w, axis=1))[0]
+        raise AssertionError(f"{name}: {bad.size} of {got.size} elements differ, first {bad[:8]}: "
+                             f"got {got[bad[:4]]} want {want[bad[:4]]}")
+
+
+# name -> (gpu call(out, first), torch dtype, oracle call(first, n), numpy view dtype)
+def fills(rng, torch, orc):
+    t = torch
+    return {
+        "u32": (lambda o, f: rng.rng_fill_u32(0x9E3779B9, f, o), t.int32,
+                lambda f, n: orc.fill_u32(0x9E3779B9, f, n).view(np.int32)),
+        "u64": (lambda o, f: rng.rng_fill_u64(0x9E3779B9, f, o), t.int64,
+                lambda f, n: orc.fill_u64(0x9E3779B9, f, n).view(np.int64)),
+        "f32": (lambda o, f: rng.rng_fill_f32(0x9E3779B9, f, o), t.float32,
+                lambda f, n: orc.fill_f32(0x9E3779B9, f, n)),
+        "f64": (lambda o, f: rng.rng_fill_f64(0x9E3779B9, f, o), t.float64,
+                lambda f, n: orc.fill_f64(0x9E3779B9, f, n)),
+        "u32_below_1000": (lambda o, f: rng.rng_fill_u32_below(1, f, 1000, o), t.int32,
+                           lambda f, n: orc.fill_u32_below(1, f, 1000, n).view(np.int32)),
+        "u32_below_2^32-2": (lambda o, f: rng.rng_fill_u32_below(2, f, U32 - 2, o), t.int32,
+                             lambda f, n: orc.fill_u32_below(2, f, U32 - 2, n).view(np.int32)),
+        "u32_below_2^31+1": (lambda o, f: rng.rng_fill_u32_below(3, f, (1 << 31) + 1, o), t.int32,
+                             lambda f, n: orc.fill_u32_below(3, f, (1 << 31) + 1, n).view(np.int32)),
+        "u64_below_1000": (lambda o, f: rng.rng_fill_u64_below(3, f, 1000, o), t.int64,
+                           lambda f, n: orc.fill_u64_below(3, f, 1000, n).view(np.int64)),
+        "u64_below_2^64-2": (lambda o, f: rng.rng_fill_u64_below(4, f, (1 << 64) - 2, o), t.int64,
+                             lambda f, n: orc.fill_u64_below(4, f, (1 << 64) - 2, n).view(np.int64)),
+        "u64_below_2^63+1": (lambda o, f: rng.rng_fill_u64_below(1, f, (1 << 63) + 1, o), t.int64,
+                             lambda f, n: orc.fill_u64_below(1, f, (1 << 63) + 1, n).view(np.int64)),
+        "i32_range": (lambda o, f: rng.rng_fill_i32_range(1, f, -500, 1000, o), t.int32,
+                      lambda f, n: orc.fill_i32_range(1, f, -500, 1000, n)),
+        "i32_range_wrap": (lambda o, f: rng.rng_fill_i32_range(2, f, (1 << 31) - 10, 1000, o), t.int32,
+                           lambda f, n: orc.fill_i32_range(2, f, (1 << 31) - 10, 1000, n)),
+        "i64_range32": (lambda o, f: rng.rng_fill_i64_range32(3, f, -500, 1000, o), t.int64,
+                        lambda f, n: orc.fill_i64_range32(3, f, -500, 1000, n)),
+        "i64_range": (lambda o, f: rng.rng_fill_i64_range(4, f, -500, 1000, o), t.int64,
+                      lambda f, n: orc.fill_i64_range(4, f, -500, 1000, n)),
+        "normal_f64": (lambda o, f: rng.rng_fill_normal_f64(7, f, o), t.float64,
+                       lambda f, n: orc.fill_normal_f64(7, f, n)),
+    }
+
+
+FILL_NAMES = ["u32", "u64", "f32", "f64", "u32_below_1000", "u32_below_2^32-2", "u32_below_2^31+1",
+              "u64_below_1000", "u64_below_2^64-2", "u64_below_2^63+1", "i32_range", "i32_range_wrap",
+              "i64_range32", "i64_range", "normal_f64"]
+
+
+@pytest.mark.parametrize("name", FILL_NAMES)
+def test_fill_bit_exact_small_and_unaligned(rng, torch, orc, name):
+    gpu, dtype, ref = fills(rng, torch, orc)[name]
+    for first in FIRSTS:
+        for offset in (0, 1):
+            for n in SMALL:
+                out = gpu(_out(torch, dtype, n, offset), first)
+                _assert_equal(f"{name} first={first} offset={offset} n={n}", _host(out), ref(first, n))
+
+
+@pytest.mark.parametrize("name", FILL_NAMES)
+def test_fill_bit_exact_several_waves(rng, torch, orc, name):
+    gpu, dtype, ref = fills(rng, torch, orc)[name]
+    for first, offset in ((0, 0), (3, 1), (U32 - 5, 0)):
+        out = gpu(_out(torch, dtype, BIG, offset), first)
+        _assert_equal(f"{name} first={first} offset={offset} n={BIG}", _host(out), ref(first, BIG))
+
+
+@pytest.mark.parametrize("name", FILL_NAMES)
+def test_fill_of_length_zero_writes_nothing(rng, torch, orc, name):
+    gpu, dtype, _ = fills(rng, torch, orc)[name]
+    guard = torch.full((4,), 7, dtype=dtype, device="cuda")
+    gpu(guard[2:2], 0)
+    torch.cuda.synchronize()
+    assert bool((guard == 7).all())
+
+
+@pytest.mark.parametrize("name", FILL_NAMES)
+def test_fill_leaves_neighbours_untouched(rng, torch, orc, name):
+    gpu, dtype, ref = fills(rng, torch, orc)[name]
+    for n, offset in ((37, 3), (4099, 1), (4096, 2)):
+        buf = torch.full((n + offset + 5,), 7, dtype=dtype, device="cuda")
+        gpu(buf[offset:offset + n], 11)
+        host = _host(buf)
+        assert np.all(host[:offset] == 7) and np.all(host[offset + n:] == 7)
+        _assert_equal(name, host[offset:offset + n], ref(11, n))
+
+
+def test_normal_f32_within_tolerance(rng, torch, orc):
+    """|z_gpu - z| <= 4e-6 (1 + |z|) against the oracle's binary64 value."""
+    for first, n, offset in ((0, 1 << 22, 0), (1, 4099, 1), (3, 65537, 0), (U32 - 5, BIG, 1)):
+        z = _host(rng.rng_fill_normal_f32(7, first, _out(torch, torch.float32, n, offset))).astype(np.float64)
+        ref = orc.fill_randn(7, first, n)
+        err = np.abs(z - ref) / (1 + np.abs(ref))
+        assert err.max() <= 4e-6, (first, n, err.max(), np.argmax(err))
+
+
+def test_normal_f32_extreme_radius(rng, torch, orc):
+    """Counters whose first uniform is the largest grid value 1 - 2^-23 (the
+    radius sqrt(46 ln 2)) and those where it is 0 (radius 0)."""
+    d = orc.fill_u32(7, 0, 1 << 26)[::2] & 0x7FFFFF
+    for target in ((1 << 23) - 1, 0, 1):
+        cs = np.nonzero(d == target)[0]
+        assert cs.size
+        out = torch.empty(1, dtype=torch.float32, device="cuda")
+        for c in cs[:4]:
+            z = float(_host(rng.rng_fill_normal_f32(7, int(c), out))[0])
+            ref = orc.randn(7, int(c))
+            assert abs(z - ref) <= 4e-6 * (1 + abs(ref))
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5, 0.0, 0.999, 2.0 ** -30])
+def test_dropout_bit_exact(rng, torch, orc, p):
+    for n, first in ((BIG, 0), (4099, U32 - 5), (1, 3), (17, 1)):
+        x = workloads.dropout_x(n)
+        dy = workloads.dropout_dy(n)
+        for offset in (0, 1):
+            xg = _out(torch, torch.float32, n, offset)
+            xg.copy_(torch.from_numpy(x))
+            y = rng.rng_dropout_fwd(xg, _out(torch, torch.float32, n, offset), p, 42, first)
+            _assert_equal(f"fwd p={p} n={n} offset={offset}", _host(y), orc.dropout(x, p, 42, first))
+            dyg = _out(torch, torch.float32, n, 1 - offset)
+            dyg.copy_(torch.from_numpy(dy))
+            dx = rng.rng_dropout_bwd(dyg, _out(torch, torch.float32, n, offset), p, 42, first)
+            _assert_equal(f"bwd p={p} n={n}", _host(dx), orc.dropout(dy, p, 42, first))
+            # the backward pass drops exactly the elements the forward pass dropped
+            both = (x != 0) & (dy != 0)
+            assert np.array_equal((_host(y) != 0)[both], (_host(dx) != 0)[both])
+
+
+def test_dropout_special_values_and_in_place(rng, torch, orc):
+    sp = workloads.special_floats()
+    x = np.tile(sp, 700)
+    for p in (0.1, 0.5):
+        want = orc.dropout(x, p, 42, 9)
+        xg = torch.from_numpy(x).cuda()
+        _assert_equal("special", _host(rng.rng_dropout_fwd(xg, torch.empty_like(xg), p, 42, 9)), want,
+                      any_nan=True)
+        rng.rng_dropout_fwd(xg, xg, p, 42, 9)  # in place
+        _assert_equal("in place", _host(xg), want, any_nan=True)
+
+
+def test_dropout_mixed_alignment_takes_the_scalar_path(rng, torch, orc):
+    n = 100003
+    x = workloads.dropout_x(n)
+    xg = _out(torch, torch.float32, n, 1)
+    xg.copy_(torch.from_numpy(x))
+    for offset in (0, 2, 3):
+        y = rng.rng_dropout_fwd(xg, _out(torch, torch.float32, n, offset), 0.5, 42, 5)
+        _assert_equal(f"mixed offset {offset}", _host(y), orc.dropout(x, 0.5, 42, 5))
+
+
+def test_slow_path_exp_log_bit_exact(rng, torch, orc):
+    """The ziggurat slow path's own exp and log, layer by layer."""
+    g = np.random.default_rng(4)
+    t = np.concatenate([g.uniform(-10, 0, 1 << 20), -np.linspace(0, 10, 4097), [0.0, -0.0]])
+    out = torch.empty(t.size, dtype=torch.float64, device="cuda")
+    _assert_equal("zexp", _host(rng.rng_debug_eval_f64(0, torch.from_numpy(t).cuda(), out)), orc.zexp_array(t))
+    x = np.concatenate([g.uniform(0, 1, 1 << 20), 2.0 ** -g.uniform(0, 53, 1 << 18),
+                        1 - g.integers(1, 1 << 20, 4096) * 2.0 ** -53, [2.0 ** -53, 0.5, 1.0]])
+    x = x[x > 0]
+    out = torch.empty(x.size, dtype=torch.float64, device="cuda")
+    _assert_equal("zlog", _host(rng.rng_debug_eval_f64(1, torch.from_numpy(x).cuda(), out)), orc.zlog_array(x))
+
+
+def test_normal_f64_miss_list_overflow_walks_the_fill(rng, torch, orc):
+    """A list too short for the misses (capacity 0 and 5) sends the second
+    kernel through the whole fill: the values must not change."""
+    n = 65537
+    want = orc.fill_normal_f64(7, 3, n)
+    try:
+        for cap in (0, 5, 300):
+            rng.rng_debug_set_miss_capacity(cap)
+            out = rng.rng_fill_normal_f64(7, 3, _out(torch, torch.float64, n, 1))
+            _assert_equal(f"capacity {cap}", _host(out), want)
+            assert rng.rng_debug_last_miss_count() > cap
+    finally:
+        rng.rng_debug_set_miss_capacity(None)
+    out = rng.rng_fill_normal_f64(7, 3, _out(torch, torch.float64, n, 0))
+    _assert_equal("default capacity", _host(out), want)
+
+
+def test_normal_f64_miss_count(rng, torch, orc):
+    """The table pass lists 0.42766 % of the elements (tandem-sycl 'Design',
+    Normals: 0.43 %), and exactly the elements the oracle's fast path misses."""
+    n = 1 << 24
+    rng.rng_fill_normal_f64(7, 0, torch.empty(n, dtype=torch.float64, device="cuda"))
+    got = rng.rng_debug_last_miss_count()
+    want = int(n - orc.fill_zig_fast(7, 0, n).astype(np.int64).sum())
+    assert got == want
+    p = 0.0042766
+    assert abs(got - p * n) < 5 * math.sqrt(p * n)
+
+
+def test_normal_f64_streams_share_the_miss_list(rng, torch, orc):
+    """Fills on two streams use the same per-device miss list in turn."""
+    n = 1 << 20
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for k in range(6):
+        s = s1 if k % 2 == 0 else s2
+        o = torch.empty(n, dtype=torch.float64, device="cuda")
+        o.record_stream(s)
+        with torch.cuda.stream(s):
+            rng.rng_fill_normal_f64(7, k * n, o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    for k, o in enumerate(outs):
+        _assert_equal(f"stream fill {k}", _host(o), orc.fill_normal_f64(7, k * n, n))
+
+
+def test_launch_counts(rng, torch):
+    o32 = torch.empty(1 << 16, dtype=torch.float32, device="cuda")
+    o64 = torch.empty(1 << 16, dtype=torch.float64, device="cuda")
+    before = rng.rng_debug_launch_count()
+    rng.rng_fill_f32(1, 0, o32)
+    rng.rng_fill_normal_f32(1, 0, o32)
+    rng.rng_dropout_fwd(o32, o32, 0.5, 1, 0)
+    assert rng.rng_debug_launch_count() - before == 3
+    before = rng.rng_debug_launch_count()
+    rng.rng_fill_normal_f64(1, 0, o64)
+    assert rng.rng_debug_launch_count() - before == 2
+
+
+def test_fill_longer_than_one_piece(rng, torch, orc):
+    """n > 2^31 is split into pieces of 2^31 elements; the seam is invisible."""
+    n = (1 << 31) + 1000
+    out = rng.rng_fill_u32(5, U32 - 7, torch.empty(n, dtype=torch.int32, device="cuda"))
+    idx = np.concatenate([np.arange(0, 64), np.arange((1 << 31) - 64, (1 << 31) + 64), np.arange(n - 64, n),
+                          np.random.default_rng(1).integers(0, n, 1 << 16)])
+    got = _host(out[torch.from_numpy(idx).cuda()])
+    _assert_equal("u32 > 2^31", got, orc.fill_u32(5, U32 - 7, idx=idx).view(np.int32))
+    del out
+    out = rng.rng_fill_normal_f64(7, 1, torch.empty(n, dtype=torch.float64, device="cuda"))
+    got = _host(out[torch.from_numpy(idx).cuda()])
+    _assert_equal("normal_f64 > 2^31", got, orc.fill_normal_f64(7, 1, idx=idx))
+    del out
+    torch.cuda.empty_cache()
+
+
+def test_bad_arguments_raise(rng, torch):
+    o = torch.empty(8, dtype=torch.float32, device="cuda")
+    with pytest.raises(rng.RngError):
+        rng.rng_dropout_fwd(o, o, 1.0, 1, 0)
+    with pytest.raises(rng.RngError):
+        rng.rng_fill_u32_below(1, 0, 0, torch.empty(8, dtype=torch.int32, device="cuda"))
+    with pytest.raises(rng.RngError):
+        rng.rng_dropout_fwd(o[:6], o[2:8], 0.5, 1, 0)
+    with pytest.raises(TypeError):
+        rng.rng_fill_u32(1, 0, torch.empty(8, dtype=torch.int32))
