@@ -174,7 +174,7 @@ def oracle_sample(orc, n_sample: int, first: int):
     return out
 
 
-def cpu_baseline(n_sample: int = 1 << 24):
+def cpu_baseline(n_sample: int = 1 << 26):
     """The oracle, single-threaded, on n_sample elements of every fill: the
     GiB/s it would write over a whole step (bytes / summed seconds)."""
     import oracle
