@@ -43,6 +43,7 @@ _FILL_SIGS = {
     "rng_fill_i64_range": [_u32, _u32, _sz, _i64, _u64, _p, _p],
     "rng_fill_normal_f32": [_u32, _u32, _sz, _p, _p],
     "rng_fill_normal_f64": [_u32, _u32, _sz, _p, _p],
+    "rng_fill_normal_f64_noalloc": [_u32, _u32, _sz, _p, _p],
     "rng_dropout_fwd": [_p, _p, _f32, _u32, _u32, _sz, _p],
     "rng_dropout_bwd": [_p, _p, _f32, _u32, _u32, _sz, _p],
     "rng_debug_set_miss_capacity": [_sz],
@@ -154,6 +155,11 @@ def rng_fill_normal_f32(seed, first_counter, out, stream=None):
 
 def rng_fill_normal_f64(seed, first_counter, out, stream=None):
     return _fill("rng_fill_normal_f64", "f64", seed, first_counter, out, stream)
+
+
+def rng_fill_normal_f64_noalloc(seed, first_counter, out, stream=None):
+    """rng_fill_normal_f64 without any device allocation (n <= 2^28); see rng.h."""
+    return _fill("rng_fill_normal_f64_noalloc", "f64", seed, first_counter, out, stream)
 
 
 def _dropout(name, x, y, p, seed, first_counter, stream):

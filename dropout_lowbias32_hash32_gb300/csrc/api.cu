@@ -235,6 +235,18 @@ rng_status rng_fill_normal_f64(uint32_t seed, uint32_t first_counter, size_t n, 
     });
 }
 
+rng_status rng_fill_normal_f64_noalloc(uint32_t seed, uint32_t first_counter, size_t n, double *out, void *stream)
+{
+    if (n > kNoAllocMaxElements)
+        return fail(RNG_EINVAL, "rng_fill_normal_f64_noalloc: n = %zu exceeds its maximum of 2^28 elements", n);
+    if (rng_status st = check_out(out, n, "out")) return st;
+    if (n == 0) return RNG_OK;
+    t_error[0] = '\0';
+    const cudaError_t e = launch_normal_f64_noalloc(seed, first_counter, static_cast<uint32_t>(n), out,
+                                                    RNG_STREAM(stream));
+    return e == cudaSuccess ? RNG_OK : cuda_fail(e, "rng_fill_normal_f64_noalloc");
+}
+
 rng_status rng_dropout_fwd(const float *x, float *y, float p, uint32_t seed, uint32_t first_counter, size_t n,
                            void *stream)
 {

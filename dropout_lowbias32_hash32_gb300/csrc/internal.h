@@ -82,4 +82,9 @@ void set_miss_capacity_override(size_t cap);
 cudaError_t last_miss_count(uint64_t *count);
 cudaError_t launch_eval_f64(int which, const double *in, double *out, uint32_t n, cudaStream_t s);
 
+// normal_f64 with the miss list in a static device array (no allocation);
+// n must not exceed kNoAllocMaxElements.
+constexpr size_t kNoAllocMaxElements = size_t(1) << 28;
+cudaError_t launch_normal_f64_noalloc(uint32_t seed, uint32_t first, uint32_t n, double *out, cudaStream_t s);
+
 }  // namespace rngk

@@ -410,4 +410,68 @@ cudaError_t launch_eval_f64(int which, const double *in, double *out, uint32_t n
     return cudaGetLastError();
 }
 
+// ---- allocation-free variant (rng_fill_normal_f64_noalloc) ------------------
+//
+// For callers that cannot call cudaMalloc: the miss counter and the miss list
+// live in this file-scope device array instead of the lazily allocated
+// per-device list above.  Layout: the 64-bit miss counter in the first 256
+// bytes, then kNoAllocListEntries 32-bit list entries (8 MiB + 256 bytes in
+// all).  Every device that loads the library holds the array until the
+// process exits, and every call shares it: two calls that overlap on the GPU
+// race on it (their outputs are then unspecified).  The counter is cleared by
+// each call before its table pass.
+
+namespace {
+
+constexpr size_t kNoAllocListEntries = size_t(1) << 21;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[256 + kNoAllocListEntries * sizeof(uint32_t)];
+
+// Device address of g_noalloc_scratch per device (host code cannot use the
+// symbol itself: on the host it names a stand-in, not device memory).
+std::atomic<unsigned char *> g_noalloc_addr[kNoAllocMaxDevices];
+std::atomic<unsigned> g_noalloc_sms[kNoAllocMaxDevices];
+
+}  // namespace
+
+cudaError_t launch_normal_f64_noalloc(uint32_t seed, uint32_t first, uint32_t n, double *out, cudaStream_t s)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+    unsigned char *scratch = g_noalloc_addr[dev].load();
+    if (scratch == nullptr) {
+        // set-up on this device's first call, with the device current
+        void *addr = nullptr;
+        if ((err = cudaGetSymbolAddress(&addr, g_noalloc_scratch)) != cudaSuccess) return err;
+        int sms = 0;
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+        g_noalloc_sms[dev].store(sms > 0 ? static_cast<unsigned>(sms) : 1u);
+        scratch = static_cast<unsigned char *>(addr);
+        g_noalloc_addr[dev].store(scratch);
+    }
+    unsigned long long *count = reinterpret_cast<unsigned long long *>(scratch);
+    uint32_t *list = reinterpret_cast<uint32_t *>(scratch + 256);
+    const size_t want = default_capacity(n);
+    const unsigned long long capacity =
+        static_cast<unsigned long long>(want < kNoAllocListEntries ? want : kNoAllocListEntries);
+
+    if ((err = cudaMemsetAsync(count, 0, sizeof(unsigned long long), s)) != cudaSuccess) return err;
+    const uint32_t key = seed_key(seed);
+    const uint32_t head = head_elems<double>(out, n);
+    const uint32_t n_vec = (n - head) / 2u;
+    const uint32_t blocks = n_vec ? (n_vec + kTableVecPerBlock - 1u) / kTableVecPerBlock : 1u;
+    zig_table_pass<<<blocks, kTableThreads, 0, s>>>(key, first, out, head, n_vec, n, list, count, capacity);
+    note_launch();
+    const uint32_t max_blocks = g_noalloc_sms[dev].load() * 4u;
+    const uint32_t want_blocks = (n + 8191u) / 8192u;
+    const uint32_t miss_blocks = want_blocks < 1u ? 1u : (want_blocks > max_blocks ? max_blocks : want_blocks);
+    zig_miss_pass<<<miss_blocks, kMissThreads, 0, s>>>(key, purpose_key(seed, kPurposeNormal64), first, out, n,
+                                                       list, count, capacity);
+    note_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace rngk

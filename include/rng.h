@@ -138,6 +138,26 @@ rng_status rng_fill_normal_f32(uint32_t seed, uint32_t first_counter, size_t n, 
 rng_status rng_fill_normal_f64(uint32_t seed, uint32_t first_counter, size_t n, double *out,
                                void *stream);
 
+/* Allocation-free variant of rng_fill_normal_f64, for callers that cannot
+ * call cudaMalloc: code whose device memory is entirely owned by another
+ * allocator (a framework's caching allocator that reserved the pool up front,
+ * where a cudaMalloc of ours would fail or fragment it), and latency-critical
+ * paths that cannot accept cudaMalloc's implicit device synchronisation.  The
+ * pages have no counterpart: it exists for those callers only.
+ *   - Same values as rng_fill_normal_f64, bit for bit.
+ *   - The miss counter and list live in one static device array of the
+ *     library (8 MiB + 256 bytes, present on every device that loads the
+ *     library until the process exits); the call makes no device allocation.
+ *   - n must not exceed 2^28 elements; larger n returns RNG_EINVAL.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the array and clears its counter first: calls whose
+ *     work overlaps on the GPU (other streams, other threads) race on it and
+ *     give unspecified values.  Order them on one stream or with events.
+ *   - Otherwise as rng_fill_normal_f64 (device pointers, stream-ordered). */
+rng_status rng_fill_normal_f64_noalloc(uint32_t seed, uint32_t first_counter, size_t n, double *out,
+                                       void *stream);
+
 /* ---- dropout (Phobos "Random numbers", section dropout) ------------------- */
 
 /* y[i] = uniform(seed, c_i) >= p ? x[i] / (1 - p) : +0, in f32 with IEEE
