@@ -10,6 +10,7 @@
 namespace rngk {
 namespace {
 
+// `key` is the folded hash of the seed (hash32.cuh).
 struct GenU32 {
     using T = uint32_t;
     uint32_t key;
@@ -33,22 +34,35 @@ struct GenF32 {
     }
 };
 
-// m * 2^-53 for m < 2^53, exactly, from integer operations only (GB300's FP64
-// pipe is far too narrow for an HBM-speed fill): normalise m so its leading
-// one sits at bit 52, which becomes the implicit bit, and add the biased
-// exponent 1022 - (clz(m) - 11) below it; the implicit bit carries into the
-// exponent field.
-__device__ __forceinline__ double scaled_u53_to_double(uint64_t m)
+// (w >> 11) * 2^-53 for the 64-bit draw w = hi:lo, exactly, from integer
+// operations only (GB300's FP64 pipe is far too narrow for an HBM-speed
+// fill).  Clear the 11 bits below m = w >> 11, normalise on the high word so
+// m's leading one reaches bit 63, take the 53-bit significand (implicit bit
+// at bit 52) and add the biased exponent 1021 - z below it; the implicit bit
+// carries one into the exponent field, giving 2^(-1-z) (1.f).  The high word
+// is zero for one draw in 2^32; such m < 2^21 go through an exact
+// integer-to-double conversion.
+__device__ __noinline__ double scaled_small_u53(uint32_t lo)
 {
-    const int lz = __clzll(m);
-    const uint64_t bits = (static_cast<uint64_t>(1032 - lz) << 52) + (m << (lz - 11));
-    return __longlong_as_double(m ? static_cast<long long>(bits) : 0ll);
+    return __dmul_rn(__uint2double_rn(lo >> 11), 0x1p-53);
+}
+
+__device__ __forceinline__ double scaled_u53_to_double(Words w)
+{
+    if (__builtin_expect(w.hi == 0, 0)) return scaled_small_u53(w.lo);
+    const uint32_t lo = w.lo & ~0x7FFu;
+    const uint32_t z = __clz(w.hi);
+    const uint32_t a_hi = __funnelshift_l(lo, w.hi, z);  // (hi:lo) << z, high word
+    const uint32_t a_lo = lo << z;
+    const uint32_t sig_hi = a_hi >> 11;  // bit 20: the implicit bit
+    const uint32_t sig_lo = __funnelshift_r(a_lo, a_hi, 11);
+    return __hiloint2double(static_cast<int>(sig_hi + ((1021u - z) << 20)), static_cast<int>(sig_lo));
 }
 
 struct GenF64 {
     using T = double;
     uint32_t key;
-    __device__ T operator()(uint32_t c) const { return scaled_u53_to_double(draw64(key, c) >> 11); }
+    __device__ T operator()(uint32_t c) const { return scaled_u53_to_double(draw64_words(key, c)); }
 };
 
 }  // namespace

@@ -27,10 +27,12 @@ void note_launch();
 // Grid of a grid-stride fill over n_vec 16-byte vectors.
 unsigned fill_blocks(uint32_t n_vec);
 
-// Seed-derived keys, computed once per fill on the host.
+// Seed-derived keys, computed once per fill on the host and passed to the
+// kernels folded (k ^ (k >> 16), see hash32.cuh).
 uint32_t host_hash32(uint32_t x);
-inline uint32_t seed_key(uint32_t seed) { return host_hash32(seed); }
-inline uint32_t purpose_key(uint32_t seed, uint32_t purpose) { return host_hash32(host_hash32(seed) ^ purpose); }
+inline uint32_t folded(uint32_t k) { return k ^ (k >> 16); }
+inline uint32_t seed_key(uint32_t seed) { return folded(host_hash32(seed)); }
+inline uint32_t purpose_key(uint32_t seed, uint32_t purpose) { return folded(host_hash32(host_hash32(seed) ^ purpose)); }
 
 constexpr uint32_t kPurposeBelow32 = 0x42333220u;  // "B32 "
 constexpr uint32_t kPurposeBelow64 = 0x42363420u;  // "B64 "

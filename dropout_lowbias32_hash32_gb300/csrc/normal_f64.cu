@@ -12,11 +12,12 @@
 // layers); the fast path makes no calls.
 //
 // Draw w = D64(seed, c): layer j = w & 1023, sign = bit 10, m = w >> 11 (53
-// bits); x = RNE((m 2^-53) X[j]); fast iff x < X[j+1].  The fast path runs at
-// HBM speed only if it stays off GB300's narrow FP64 pipe, so the rounded
-// product is formed with integer multiplies (bit-identical to the IEEE
-// multiply; the miss pass, which runs for 0.43 % of elements, uses the FP64
-// pipe for the same product).
+// bits); x = RNE((m 2^-53) X[j]); fast iff x < X[j+1].  GB300's FP64 pipe
+// retires 2 fma per SM and cycle (1/64 of FP32), so the fast path spends
+// exactly one FP64 instruction per element: t = 1 + (m mod 2^52) 2^-52 is
+// assembled from the draw's bits, and fma(t, X[j]/2, b ? 0 : -X[j]/2) with
+// b = bit 52 of m equals (m 2^-53) X[j] before its single rounding, so it
+// returns the IEEE product bit for bit.
 //
 // Miss of layer 0: the tail beyond r = X[1] (Marsaglia 1964: a = -log(U1)/r,
 // b = -log(U2), accept when 2b >= a^2, value r + a, U in (0, 1]).  Miss of
@@ -47,7 +48,7 @@ constexpr uint32_t kLayers = 1024;
 // Layer table, global memory, read through the read-only path.
 __device__ const double kZigX[kLayers + 1] = {ZIG_X_VALUES};
 __device__ const double kZigF[kLayers + 1] = {ZIG_F_VALUES};
-__device__ const double2 kZigXPair[kLayers] = {ZIG_XPAIR_VALUES};
+__device__ const double2 kZigHalfXNext[kLayers] = {ZIG_HALFX_XNEXT_VALUES};  // {X[j]/2, X[j+1]}
 
 constexpr uint32_t kTableThreads = 256;
 constexpr uint32_t kTableIters = 8;  // 16-byte vectors per thread and block
@@ -58,42 +59,29 @@ constexpr uint32_t kMaxRounds = 4096;  // rejection rounds of one miss (never re
 
 // ---- fast path ------------------------------------------------------------
 
-// Bits of RNE((m 2^-53) X) for 1 <= m < 2^53 and X a positive normal double
-// with biased exponent E and significand S (2^52 <= S < 2^53): normalise m to
-// a = m << z (leading one at bit 63); the 117-bit a S has its leading one at
-// bit 116 or 115 of (hi, lo); keep 53 bits q, round to nearest even on the
-// bits below, and assemble exponent E - z + 9 (+1 when the leading one is at
-// bit 116) with q's implicit bit carrying into it (also when rounding
-// carries q to 2^53).
-__device__ __forceinline__ uint64_t mul_u53_bits(uint64_t m, uint64_t xbits)
-{
-    const uint64_t sig = (xbits & 0x000FFFFFFFFFFFFFull) | 0x0010000000000000ull;
-    const uint32_t e = static_cast<uint32_t>(xbits >> 52);
-    const uint32_t z = __clzll(m);
-    const uint64_t a = m << z;
-    const uint64_t hi = __umul64hi(a, sig);
-    const uint64_t lo = a * sig;
-    const uint32_t top = static_cast<uint32_t>(hi >> 52);  // 1: leading one at bit 116
-    const uint64_t q = top ? hi : ((hi << 1) | (lo >> 63));
-    const uint64_t rest = top ? lo : (lo << 1);  // discarded bits, left-aligned
-    const uint64_t up = (rest >> 63) & static_cast<uint64_t>(((rest << 1) != 0) | (q & 1u));
-    return (static_cast<uint64_t>(e - z + 9u + top) << 52) + q + up;
-}
-
 struct FastDraw {
     uint64_t bits;  // the signed fast-path value
     bool fast;
 };
 
-__device__ __forceinline__ FastDraw zig_fast(uint64_t w)
+// Fast path of the 64-bit draw w = hi:lo (see the file comment).
+__device__ __forceinline__ FastDraw zig_fast(Words w)
 {
-    const double2 edges = __ldg(&kZigXPair[static_cast<uint32_t>(w) & (kLayers - 1u)]);
-    const uint64_t m = w >> 11;
-    const uint64_t mag = m ? mul_u53_bits(m, static_cast<uint64_t>(__double_as_longlong(edges.x))) : 0ull;
+    const double2 e = __ldg(&kZigHalfXNext[w.lo & (kLayers - 1u)]);
+    // t = 1 + (m mod 2^52) 2^-52, m = (hi:lo) >> 11
+    const uint32_t t_lo = __funnelshift_r(w.lo, w.hi, 11);
+    const uint32_t t_hi = ((w.hi >> 11) & 0xFFFFFu) | 0x3FF00000u;
+    // addend 0 when bit 52 of m (bit 31 of hi) is set, else -X[j]/2
+    const uint32_t keep = static_cast<uint32_t>(static_cast<int32_t>(w.hi) >> 31);
+    const uint32_t c_hi = (static_cast<uint32_t>(__double2hiint(e.x)) ^ 0x80000000u) & ~keep;
+    const uint32_t c_lo = static_cast<uint32_t>(__double2loint(e.x)) & ~keep;
+    const double x = __fma_rn(__hiloint2double(static_cast<int>(t_hi), static_cast<int>(t_lo)), e.x,
+                              __hiloint2double(static_cast<int>(c_hi), static_cast<int>(c_lo)));
+    const uint64_t xb = static_cast<uint64_t>(__double_as_longlong(x));
     FastDraw d;
     // both values are non-negative, so their bit patterns order like them
-    d.fast = mag < static_cast<uint64_t>(__double_as_longlong(edges.y));
-    d.bits = mag | ((w << 53) & 0x8000000000000000ull);  // bit 10 -> sign bit
+    d.fast = xb < static_cast<uint64_t>(__double_as_longlong(e.y));
+    d.bits = xb | (static_cast<uint64_t>(w.lo & 0x400u) << 53);  // bit 10 -> sign bit
     return d;
 }
 
@@ -230,8 +218,8 @@ zig_table_pass(uint32_t key, uint32_t first, double *__restrict__ out, uint32_t 
         const uint32_t e0 = head + 2u * v;
         bool miss0 = false, miss1 = false;
         if (v < n_vec) {
-            const FastDraw a = zig_fast(draw64(key, first + e0));
-            const FastDraw b = zig_fast(draw64(key, first + e0 + 1u));
+            const FastDraw a = zig_fast(draw64_words(key, first + e0));
+            const FastDraw b = zig_fast(draw64_words(key, first + e0 + 1u));
             const uint4 u = make_uint4(static_cast<uint32_t>(a.bits), static_cast<uint32_t>(a.bits >> 32),
                                        static_cast<uint32_t>(b.bits), static_cast<uint32_t>(b.bits >> 32));
             __stcs(reinterpret_cast<uint4 *>(out + e0), u);
@@ -255,7 +243,7 @@ zig_table_pass(uint32_t key, uint32_t first, double *__restrict__ out, uint32_t 
         }
         bool miss = false;
         if (here) {
-            const FastDraw d = zig_fast(draw64(key, first + e));
+            const FastDraw d = zig_fast(draw64_words(key, first + e));
             out[e] = __longlong_as_double(static_cast<long long>(d.bits));
             miss = !d.fast;
         }
@@ -293,7 +281,7 @@ zig_miss_pass(uint32_t key, uint32_t normal_key, uint32_t first, double *__restr
         }
     } else {
         for (uint32_t e = tid; e < n; e += stride)
-            if (!zig_fast(draw64(key, first + e)).fast) out[e] = zig_slow(key, normal_key, first + e);
+            if (!zig_fast(draw64_words(key, first + e)).fast) out[e] = zig_slow(key, normal_key, first + e);
     }
 }
 
