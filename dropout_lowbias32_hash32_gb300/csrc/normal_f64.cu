@@ -11,6 +11,11 @@
 // global memory (constant memory serialises lanes that read different
 // layers); the fast path makes no calls.
 //
+// Misses of the base layer (1.3 % of misses) need two logarithms and a
+// division, the others (wedges) one exponential: the table pass keeps them in
+// two lists so that the miss pass runs each kind in dense warps instead of
+// holding a warp of wedges for one tail lane.
+//
 // Draw w = D64(seed, c): layer j = w & 1023, sign = bit 10, m = w >> 11 (53
 // bits); x = RNE((m 2^-53) X[j]); fast iff x < X[j+1].  GB300's FP64 pipe
 // retires 2 fma per SM and cycle (1/64 of FP32), so the fast path spends
@@ -47,54 +52,78 @@ constexpr uint32_t kLayers = 1024;
 
 // Layer table, global memory, read through the read-only path.
 __device__ const double kZigX[kLayers + 1] = {ZIG_X_VALUES};
-__device__ const double kZigF[kLayers + 1] = {ZIG_F_VALUES};
 __device__ const double2 kZigHalfXNext[kLayers] = {ZIG_HALFX_XNEXT_VALUES};  // {X[j]/2, X[j+1]}
+__device__ const double2 kZigFHalfDiff[kLayers] = {ZIG_F_HALFDIFF_VALUES};   // {F[j], (F[j+1]-F[j])/2}
 
 constexpr uint32_t kTableThreads = 256;
 constexpr uint32_t kTableIters = 8;  // 16-byte vectors per thread and block
 constexpr uint32_t kTableVecPerBlock = kTableThreads * kTableIters;  // 4096 elements
-constexpr uint32_t kQueue = 1024;  // per-block miss queue (17.5 misses expected per block)
+constexpr uint32_t kWedgeQueue = 1024;  // per-block queues (17.5 and 0.23 misses expected)
+constexpr uint32_t kTailQueue = 64;
 constexpr uint32_t kMissThreads = 128;
+constexpr uint32_t kMissBlocksPerSm = 8;
 constexpr uint32_t kMaxRounds = 4096;  // rejection rounds of one miss (never reached)
 
+// Where the table pass lists its misses: counts[0] wedge misses, counts[1]
+// base-layer (tail) misses; a count above its capacity means the list
+// overflowed and the miss pass walks the whole fill.
+struct MissList {
+    unsigned long long *counts;
+    uint32_t *wedge;
+    uint32_t *tail;
+    unsigned long long wedge_cap, tail_cap;
+};
+
 // ---- fast path ------------------------------------------------------------
+
+// RNE((m 2^-53) v) for the 64-bit word w = hi:lo, m = w >> 11, from half_v =
+// v/2 (v positive normal), in one fma: t = 1 + (m mod 2^52) 2^-52 is
+// assembled from the word's bits; with b = bit 52 of m, t v/2 - (1 - b) v/2
+// = (m 2^-53) v exactly, and the fma rounds that value once.
+__device__ __forceinline__ double scaled_by_u53(Words w, double half_v)
+{
+    const uint32_t t_lo = __funnelshift_r(w.lo, w.hi, 11);
+    const uint32_t t_hi = ((w.hi >> 11) & 0xFFFFFu) | 0x3FF00000u;
+    const uint32_t keep = static_cast<uint32_t>(static_cast<int32_t>(w.hi) >> 31);  // all ones iff b
+    const uint32_t c_hi = (static_cast<uint32_t>(__double2hiint(half_v)) ^ 0x80000000u) & ~keep;
+    const uint32_t c_lo = static_cast<uint32_t>(__double2loint(half_v)) & ~keep;
+    return __fma_rn(__hiloint2double(static_cast<int>(t_hi), static_cast<int>(t_lo)), half_v,
+                    __hiloint2double(static_cast<int>(c_hi), static_cast<int>(c_lo)));
+}
 
 struct FastDraw {
     uint64_t bits;  // the signed fast-path value
     bool fast;
+    bool base;      // the draw's layer is 0 (a miss goes to the tail)
 };
 
-// Fast path of the 64-bit draw w = hi:lo (see the file comment).
 __device__ __forceinline__ FastDraw zig_fast(Words w)
 {
-    const double2 e = __ldg(&kZigHalfXNext[w.lo & (kLayers - 1u)]);
-    // t = 1 + (m mod 2^52) 2^-52, m = (hi:lo) >> 11
-    const uint32_t t_lo = __funnelshift_r(w.lo, w.hi, 11);
-    const uint32_t t_hi = ((w.hi >> 11) & 0xFFFFFu) | 0x3FF00000u;
-    // addend 0 when bit 52 of m (bit 31 of hi) is set, else -X[j]/2
-    const uint32_t keep = static_cast<uint32_t>(static_cast<int32_t>(w.hi) >> 31);
-    const uint32_t c_hi = (static_cast<uint32_t>(__double2hiint(e.x)) ^ 0x80000000u) & ~keep;
-    const uint32_t c_lo = static_cast<uint32_t>(__double2loint(e.x)) & ~keep;
-    const double x = __fma_rn(__hiloint2double(static_cast<int>(t_hi), static_cast<int>(t_lo)), e.x,
-                              __hiloint2double(static_cast<int>(c_hi), static_cast<int>(c_lo)));
-    const uint64_t xb = static_cast<uint64_t>(__double_as_longlong(x));
+    const uint32_t j = w.lo & (kLayers - 1u);
+    const double2 e = __ldg(&kZigHalfXNext[j]);
+    const uint64_t xb = static_cast<uint64_t>(__double_as_longlong(scaled_by_u53(w, e.x)));
     FastDraw d;
     // both values are non-negative, so their bit patterns order like them
     d.fast = xb < static_cast<uint64_t>(__double_as_longlong(e.y));
     d.bits = xb | (static_cast<uint64_t>(w.lo & 0x400u) << 53);  // bit 10 -> sign bit
+    d.base = j == 0;
     return d;
 }
 
 // ---- slow path --------------------------------------------------------------
 
-// exp(t) for t in [-10, 0]: k = rint(t / ln 2), r = t - k ln 2 by two fma
-// (ln 2 = ln2_high + ln2_low, ln2_high with 32 significant bits), degree-13
-// Taylor polynomial in Horner form, exact scaling by 2^k.
+// exp(t) for t in [-10, 0]: k = rint(t / ln 2) (the rounding done by adding
+// and subtracting 1.5 2^52, which rounds to the nearest even integer exactly
+// as rint does for |t / ln 2| < 2^51), r = t - k ln 2 by two fma (ln 2 =
+// ln2_high + ln2_low, ln2_high with 32 significant bits), degree-13 Taylor
+// polynomial in Horner form, exact scaling by 2^k on the exponent field.
 __device__ __forceinline__ double zexp(double t)
 {
-    const double k = rint(__dmul_rn(t, ZK_INV_LN2));
-    double r = __fma_rn(-k, ZK_LN2_HIGH, t);
-    r = __fma_rn(-k, ZK_LN2_LOW, r);
+    const double shifted = __dadd_rn(__dmul_rn(t, ZK_INV_LN2), 0x1.8p52);
+    const int k = __double2loint(shifted);  // low word of 1.5 2^52 + k is k
+    const double kd = __dsub_rn(shifted, 0x1.8p52);
+    double r = __fma_rn(-kd, ZK_LN2_HIGH, t);
+    r = __fma_rn(-kd, ZK_LN2_LOW, r);
     double p = ZK_INV_FACT_13;
     p = __fma_rn(p, r, ZK_INV_FACT_12);
     p = __fma_rn(p, r, ZK_INV_FACT_11);
@@ -109,8 +138,8 @@ __device__ __forceinline__ double zexp(double t)
     p = __fma_rn(p, r, ZK_INV_FACT_2);
     p = __fma_rn(p, r, ZK_INV_FACT_1);
     p = __fma_rn(p, r, ZK_INV_FACT_0);
-    const double scale = __longlong_as_double(static_cast<long long>(1023 + static_cast<int>(k)) << 52);
-    return __dmul_rn(p, scale);
+    const uint64_t scale = static_cast<uint64_t>(static_cast<int64_t>(k)) << 52;  // k in [-15, 0]
+    return __longlong_as_double(static_cast<long long>(static_cast<uint64_t>(__double_as_longlong(p)) + scale));
 }
 
 // log(x) for positive normal x: x = 2^e m with m in (sqrt(1/2), sqrt 2],
@@ -144,25 +173,32 @@ __device__ __forceinline__ double zlog(double x)
     return __fma_rn(de, ZK_LN2_HIGH, __fma_rn(de, ZK_LN2_LOW, log_m));
 }
 
-__device__ __forceinline__ double u53(uint64_t w) { return __dmul_rn(__ull2double_rn(w >> 11), 0x1p-53); }
+// ((w >> 11) + 1) 2^-53, in (0, 1]
+__device__ __forceinline__ double u53_open(Words w)
+{
+    const uint64_t m = ((static_cast<uint64_t>(w.hi) << 32 | w.lo) >> 11) + 1u;
+    return __dmul_rn(__ull2double_rn(m), 0x1p-53);
+}
 
 // The value of element counter c whose first draw missed the fast path
-// (also correct, if slower, for one that did not).
+// (also correct, if slower, for one that did not).  skf is the element's
+// substream key, folded: its 64-bit word k is draw64_words(skf, k).
 __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint32_t c)
 {
-    uint64_t w = draw64(key, c);
-    const uint32_t skey = substream_key(normal_key, c);
+    Words w = draw64_words(key, c);
+    const uint32_t skf = fold_key(substream_key(normal_key, c));
     uint32_t k = 0;
     for (uint32_t round = 0; round < kMaxRounds; ++round) {
-        const uint32_t j = static_cast<uint32_t>(w) & (kLayers - 1u);
-        const bool neg = (w >> 10) & 1u;
-        const double x = __dmul_rn(u53(w), kZigX[j]);
-        if (x < kZigX[j + 1]) return neg ? -x : x;
+        const uint32_t j = w.lo & (kLayers - 1u);
+        const bool neg = w.lo & 0x400u;
+        const double2 e = __ldg(&kZigHalfXNext[j]);
+        const double x = scaled_by_u53(w, e.x);
+        if (__double_as_longlong(x) < __double_as_longlong(e.y)) return neg ? -x : x;
         if (j == 0) {
             const double r = kZigX[1];
             for (uint32_t t = 0; t < kMaxRounds; ++t) {
-                const double u1 = __dmul_rn(__ull2double_rn((substream64(skey, k) >> 11) + 1u), 0x1p-53);
-                const double u2 = __dmul_rn(__ull2double_rn((substream64(skey, k + 1u) >> 11) + 1u), 0x1p-53);
+                const double u1 = u53_open(draw64_words(skf, k));
+                const double u2 = u53_open(draw64_words(skf, k + 1u));
                 k += 2u;
                 const double a = __ddiv_rn(-zlog(u1), r);
                 const double b = -zlog(u2);
@@ -173,12 +209,12 @@ __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint3
             }
             break;
         }
-        const double u = u53(substream64(skey, k));
+        const double2 f = __ldg(&kZigFHalfDiff[j]);
+        const double y = __dadd_rn(f.x, scaled_by_u53(draw64_words(skf, k), f.y));
         k += 1u;
-        const double y = __dadd_rn(kZigF[j], __dmul_rn(u, __dsub_rn(kZigF[j + 1], kZigF[j])));
         const double t = __dmul_rn(__dmul_rn(x, x), -0.5);
         if (y < zexp(t)) return neg ? -x : x;
-        w = substream64(skey, k);
+        w = draw64_words(skf, k);
         k += 1u;
     }
     return __longlong_as_double(0x7FF8000000000000ll);
@@ -186,28 +222,40 @@ __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint3
 
 // ---- kernels -----------------------------------------------------------------
 
+// warp-aggregated append of the lanes in `ballot` (this lane if `mine`) to a
+// shared queue
+__device__ __forceinline__ void queue_append(uint32_t ballot, bool mine, uint32_t e, uint32_t *queue,
+                                             uint32_t *queued, uint32_t capacity)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+    uint32_t slot0 = 0;
+    if (lane == 0) slot0 = atomicAdd(queued, static_cast<uint32_t>(__popc(ballot)));
+    slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
+    if (mine) {
+        const uint32_t slot = slot0 + __popc(ballot & ((1u << lane) - 1u));
+        if (slot < capacity) queue[slot] = e;
+    }
+}
+
 __global__ void __launch_bounds__(kTableThreads)
 zig_table_pass(uint32_t key, uint32_t first, double *__restrict__ out, uint32_t head, uint32_t n_vec, uint32_t n,
-               uint32_t *__restrict__ list, unsigned long long *__restrict__ count, unsigned long long capacity)
+               MissList ml)
 {
-    __shared__ uint32_t queue[kQueue];
-    __shared__ uint32_t queued;
-    __shared__ unsigned long long base;
-    if (threadIdx.x == 0) queued = 0;
+    __shared__ uint32_t wedge_q[kWedgeQueue];
+    __shared__ uint32_t tail_q[kTailQueue];
+    __shared__ uint32_t wedge_n, tail_n;
+    __shared__ unsigned long long wedge_base, tail_base;
+    if (threadIdx.x == 0) wedge_n = tail_n = 0;
     __syncthreads();
-    const uint32_t lane = threadIdx.x & 31u;
 
-    // warp-aggregated append of the lanes' misses to the block's queue
-    auto push = [&](bool miss, uint32_t e) {
-        const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, miss);
-        if (ballot) {
-            uint32_t slot0 = 0;
-            if (lane == 0) slot0 = atomicAdd(&queued, static_cast<uint32_t>(__popc(ballot)));
-            slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
-            if (miss) {
-                const uint32_t slot = slot0 + __popc(ballot & ((1u << lane) - 1u));
-                if (slot < kQueue) queue[slot] = e;
-            }
+    auto push = [&](const FastDraw &d, bool valid, uint32_t e) {
+        const bool miss = valid && !d.fast;
+        const uint32_t any = __ballot_sync(0xFFFFFFFFu, miss);
+        if (any) {
+            const bool tail = miss && d.base;
+            const uint32_t tails = __ballot_sync(0xFFFFFFFFu, tail);
+            queue_append(any & ~tails, miss && !tail, e, wedge_q, &wedge_n, kWedgeQueue);
+            if (tails) queue_append(tails, tail, e, tail_q, &tail_n, kTailQueue);
         }
     };
 
@@ -216,18 +264,17 @@ zig_table_pass(uint32_t key, uint32_t first, double *__restrict__ out, uint32_t 
     for (uint32_t it = 0; it < kTableIters; ++it) {
         const uint32_t v = v_begin + it * kTableThreads + threadIdx.x;
         const uint32_t e0 = head + 2u * v;
-        bool miss0 = false, miss1 = false;
-        if (v < n_vec) {
-            const FastDraw a = zig_fast(draw64_words(key, first + e0));
-            const FastDraw b = zig_fast(draw64_words(key, first + e0 + 1u));
+        const bool valid = v < n_vec;
+        FastDraw a{}, b{};
+        if (valid) {
+            a = zig_fast(draw64_words(key, first + e0));
+            b = zig_fast(draw64_words(key, first + e0 + 1u));
             const uint4 u = make_uint4(static_cast<uint32_t>(a.bits), static_cast<uint32_t>(a.bits >> 32),
                                        static_cast<uint32_t>(b.bits), static_cast<uint32_t>(b.bits >> 32));
             __stcs(reinterpret_cast<uint4 *>(out + e0), u);
-            miss0 = !a.fast;
-            miss1 = !b.fast;
         }
-        push(miss0, e0);
-        push(miss1, e0 + 1u);
+        push(a, valid, e0);
+        push(b, valid, e0 + 1u);
     }
     // the peeled head and tail (at most one element each), by warp 0 of block 0
     if (blockIdx.x == 0 && threadIdx.x < 32u) {
@@ -241,42 +288,47 @@ zig_table_pass(uint32_t key, uint32_t first, double *__restrict__ out, uint32_t 
             e = tail0;
             here = true;
         }
-        bool miss = false;
+        FastDraw d{};
         if (here) {
-            const FastDraw d = zig_fast(draw64_words(key, first + e));
+            d = zig_fast(draw64_words(key, first + e));
             out[e] = __longlong_as_double(static_cast<long long>(d.bits));
-            miss = !d.fast;
         }
-        push(miss, e);
+        push(d, here, e);
     }
     __syncthreads();
-    const uint32_t total = queued;
-    if (total == 0) return;
-    // one atomic per block; a full queue forces the count past the capacity,
-    // which sends the miss pass through the whole-fill walk
-    if (threadIdx.x == 0)
-        base = atomicAdd(count, total <= kQueue ? static_cast<unsigned long long>(total) : capacity + 1ull);
+    const uint32_t nw = wedge_n, nt = tail_n;
+    if (nw == 0 && nt == 0) return;
+    // one atomic per list and block; a full queue forces the count past the
+    // capacity, which sends the miss pass through the whole-fill walk
+    if (threadIdx.x == 0) {
+        if (nw) wedge_base = atomicAdd(&ml.counts[0], nw <= kWedgeQueue ? nw : ml.wedge_cap + 1ull);
+        if (nt) tail_base = atomicAdd(&ml.counts[1], nt <= kTailQueue ? nt : ml.tail_cap + 1ull);
+    }
     __syncthreads();
-    if (total <= kQueue) {
-        for (uint32_t i = threadIdx.x; i < total; i += kTableThreads) {
-            const unsigned long long slot = base + i;
-            if (slot < capacity) list[slot] = queue[i];
-        }
+    if (nw && nw <= kWedgeQueue) {
+        for (uint32_t i = threadIdx.x; i < nw; i += kTableThreads)
+            if (wedge_base + i < ml.wedge_cap) ml.wedge[wedge_base + i] = wedge_q[i];
+    }
+    if (nt && nt <= kTailQueue) {
+        for (uint32_t i = threadIdx.x; i < nt; i += kTableThreads)
+            if (tail_base + i < ml.tail_cap) ml.tail[tail_base + i] = tail_q[i];
     }
 }
 
 __global__ void __launch_bounds__(kMissThreads)
 zig_miss_pass(uint32_t key, uint32_t normal_key, uint32_t first, double *__restrict__ out, uint32_t n,
-              const uint32_t *__restrict__ list, const unsigned long long *__restrict__ count,
-              unsigned long long capacity)
+              MissList ml)
 {
-    const unsigned long long misses = *count;
+    const unsigned long long nw = ml.counts[0], nt = ml.counts[1];
     const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
     const uint32_t stride = gridDim.x * blockDim.x;
-    if (misses <= capacity) {
-        const uint32_t m = static_cast<uint32_t>(misses);
-        for (uint32_t i = tid; i < m; i += stride) {
-            const uint32_t e = list[i];
+    if (nw <= ml.wedge_cap && nt <= ml.tail_cap) {
+        for (uint32_t i = tid; i < nw; i += stride) {
+            const uint32_t e = ml.wedge[i];
+            out[e] = zig_slow(key, normal_key, first + e);
+        }
+        for (uint32_t i = tid; i < nt; i += stride) {
+            const uint32_t e = ml.tail[i];
             out[e] = zig_slow(key, normal_key, first + e);
         }
     } else {
@@ -292,15 +344,51 @@ __global__ void eval_f64_kernel(int which, const double *in, double *out, uint32
         out[i] = which ? zlog(in[i]) : zexp(in[i]);
 }
 
+// Expected misses of n elements (p = 0.42766 %, of which the base layer's
+// 5.36e-5) plus 16 standard deviations and slack.
+size_t wedge_capacity(uint32_t n)
+{
+    const double mean = static_cast<double>(n) * 0.0042766;
+    return static_cast<size_t>(mean + 16.0 * std::sqrt(mean + 1.0) + 4096.0);
+}
+
+size_t tail_capacity(uint32_t n)
+{
+    const double mean = static_cast<double>(n) * 5.36e-5;
+    return static_cast<size_t>(mean + 16.0 * std::sqrt(mean + 1.0) + 1024.0);
+}
+
+// Table pass + miss pass of one piece into the lists of `ml` (counts cleared
+// here first).
+cudaError_t enqueue_ziggurat(uint32_t seed, uint32_t first, uint32_t n, double *out, const MissList &ml,
+                             unsigned sms, cudaStream_t s)
+{
+    cudaError_t err = cudaMemsetAsync(ml.counts, 0, 2 * sizeof(unsigned long long), s);
+    if (err != cudaSuccess) return err;
+    const uint32_t key = seed_key(seed);
+    const uint32_t head = head_elems<double>(out, n);
+    const uint32_t n_vec = (n - head) / 2u;
+    const uint32_t blocks = n_vec ? (n_vec + kTableVecPerBlock - 1u) / kTableVecPerBlock : 1u;
+    zig_table_pass<<<blocks, kTableThreads, 0, s>>>(key, first, out, head, n_vec, n, ml);
+    note_launch();
+    const uint32_t max_blocks = sms * kMissBlocksPerSm;
+    const uint32_t want_blocks = (n + 4095u) / 4096u;
+    const uint32_t miss_blocks = want_blocks < 1u ? 1u : (want_blocks > max_blocks ? max_blocks : want_blocks);
+    zig_miss_pass<<<miss_blocks, kMissThreads, 0, s>>>(key, purpose_key(seed, kPurposeNormal64), first, out, n, ml);
+    note_launch();
+    return cudaGetLastError();
+}
+
 // ---- per-device resources -------------------------------------------------
 
-// The miss list and its counter, allocated on first use and kept to the end
-// of the process; fills sharing them are ordered through `last`.
+// The miss lists and their counters, allocated on first use (grown when a
+// longer fill needs more) and kept to the end of the process; fills sharing
+// them are ordered through `last`.
 struct ZigDevice {
     std::mutex mu;
-    uint32_t *list = nullptr;
-    unsigned long long *count = nullptr;
-    size_t allocated = 0;
+    unsigned char *buffer = nullptr;  // counters (256 bytes), wedge list, tail list
+    size_t wedge_alloc = 0, tail_alloc = 0;
+    unsigned long long *counts = nullptr;
     cudaEvent_t last = nullptr;
     bool recorded = false;
 };
@@ -317,13 +405,6 @@ ZigDevice &device_state(int dev)
     return *slot;
 }
 
-// Expected misses n p (p = 0.42766 %) plus 16 standard deviations and slack.
-size_t default_capacity(uint32_t n)
-{
-    const double mean = static_cast<double>(n) * 0.0042766;
-    return static_cast<size_t>(mean + 16.0 * std::sqrt(mean + 1.0) + 4096.0);
-}
-
 }  // namespace
 
 void set_miss_capacity_override(size_t cap) { g_capacity_override.store(cap); }
@@ -336,38 +417,33 @@ cudaError_t launch_normal_f64(uint32_t seed, uint32_t first, uint32_t n, double 
     ZigDevice &z = device_state(dev);
     std::lock_guard<std::mutex> lock(z.mu);
 
-    const size_t want = default_capacity(n);
+    const size_t want_w = wedge_capacity(n), want_t = tail_capacity(n);
     if (!z.last && (err = cudaEventCreateWithFlags(&z.last, cudaEventDisableTiming)) != cudaSuccess) return err;
-    if (!z.count && cudaMalloc(&z.count, sizeof(unsigned long long)) != cudaSuccess)
-        return cudaErrorMemoryAllocation;
-    if (z.allocated < want) {
+    if (z.wedge_alloc < want_w || z.tail_alloc < want_t) {
         if (z.recorded && (err = cudaEventSynchronize(z.last)) != cudaSuccess) return err;
-        if (z.list) cudaFree(z.list);
-        z.list = nullptr;
-        z.allocated = 0;
-        if (cudaMalloc(&z.list, want * sizeof(uint32_t)) != cudaSuccess) return cudaErrorMemoryAllocation;
-        z.allocated = want;
+        const size_t w = want_w > z.wedge_alloc ? want_w : z.wedge_alloc;
+        const size_t t = want_t > z.tail_alloc ? want_t : z.tail_alloc;
+        if (z.buffer) cudaFree(z.buffer);
+        z.buffer = nullptr;
+        z.wedge_alloc = z.tail_alloc = 0;
+        if (cudaMalloc(&z.buffer, 256 + (w + t) * sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();  // an allocation failure is not sticky: clear it
+            return cudaErrorMemoryAllocation;
+        }
+        z.wedge_alloc = w;
+        z.tail_alloc = t;
+        z.counts = reinterpret_cast<unsigned long long *>(z.buffer);
     }
-    const size_t cap_override = g_capacity_override.load();
-    const unsigned long long capacity = static_cast<unsigned long long>(want < cap_override ? want : cap_override);
+    const size_t cap = g_capacity_override.load();
+    MissList ml;
+    ml.counts = z.counts;
+    ml.wedge = reinterpret_cast<uint32_t *>(z.buffer + 256);
+    ml.tail = ml.wedge + z.wedge_alloc;
+    ml.wedge_cap = static_cast<unsigned long long>(want_w < cap ? want_w : cap);
+    ml.tail_cap = static_cast<unsigned long long>(want_t < cap ? want_t : cap);
 
     if (z.recorded && (err = cudaStreamWaitEvent(s, z.last, 0)) != cudaSuccess) return err;
-    if ((err = cudaMemsetAsync(z.count, 0, sizeof(unsigned long long), s)) != cudaSuccess) return err;
-
-    const uint32_t key = seed_key(seed);
-    const uint32_t head = head_elems<double>(out, n);
-    const uint32_t n_vec = (n - head) / 2u;
-    const uint32_t blocks = n_vec ? (n_vec + kTableVecPerBlock - 1u) / kTableVecPerBlock : 1u;
-    zig_table_pass<<<blocks, kTableThreads, 0, s>>>(key, first, out, head, n_vec, n, z.list, z.count, capacity);
-    note_launch();
-
-    const uint32_t max_blocks = sm_count() * 4u;
-    const uint32_t want_blocks = (n + 8191u) / 8192u;
-    const uint32_t miss_blocks = want_blocks < 1u ? 1u : (want_blocks > max_blocks ? max_blocks : want_blocks);
-    zig_miss_pass<<<miss_blocks, kMissThreads, 0, s>>>(key, purpose_key(seed, kPurposeNormal64), first, out, n,
-                                                       z.list, z.count, capacity);
-    note_launch();
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = enqueue_ziggurat(seed, first, n, out, ml, sm_count(), s)) != cudaSuccess) return err;
     if ((err = cudaEventRecord(z.last, s)) != cudaSuccess) return err;
     z.recorded = true;
     return cudaSuccess;
@@ -385,9 +461,9 @@ cudaError_t last_miss_count(uint64_t *count)
         return cudaSuccess;
     }
     if ((err = cudaEventSynchronize(z.last)) != cudaSuccess) return err;
-    unsigned long long c = 0;
-    err = cudaMemcpy(&c, z.count, sizeof c, cudaMemcpyDeviceToHost);
-    *count = c;
+    unsigned long long c[2] = {0, 0};
+    err = cudaMemcpy(c, z.counts, sizeof c, cudaMemcpyDeviceToHost);
+    *count = c[0] + c[1];
     return err;
 }
 
@@ -400,21 +476,23 @@ cudaError_t launch_eval_f64(int which, const double *in, double *out, uint32_t n
 
 // ---- allocation-free variant (rng_fill_normal_f64_noalloc) ------------------
 //
-// For callers that cannot call cudaMalloc: the miss counter and the miss list
-// live in this file-scope device array instead of the lazily allocated
-// per-device list above.  Layout: the 64-bit miss counter in the first 256
-// bytes, then kNoAllocListEntries 32-bit list entries (8 MiB + 256 bytes in
-// all).  Every device that loads the library holds the array until the
-// process exits, and every call shares it: two calls that overlap on the GPU
-// race on it (their outputs are then unspecified).  The counter is cleared by
-// each call before its table pass.
+// For callers that cannot call cudaMalloc: the miss counters and lists live
+// in this file-scope device array instead of the lazily allocated per-device
+// buffer above.  Layout: the two 64-bit miss counters in the first 256 bytes,
+// then kNoAllocWedgeEntries wedge entries and kNoAllocTailEntries tail
+// entries of 32 bits (8 MiB + 256 bytes in all).  Every device that loads the
+// library holds the array until the process exits, and every call shares it:
+// two calls that overlap on the GPU race on it (their outputs are then
+// unspecified).  The counters are cleared by each call before its table pass.
 
 namespace {
 
-constexpr size_t kNoAllocListEntries = size_t(1) << 21;
+constexpr size_t kNoAllocTailEntries = size_t(1) << 16;
+constexpr size_t kNoAllocWedgeEntries = (size_t(1) << 21) - kNoAllocTailEntries;
 constexpr int kNoAllocMaxDevices = 64;
 
-static __device__ __align__(256) unsigned char g_noalloc_scratch[256 + kNoAllocListEntries * sizeof(uint32_t)];
+static __device__ __align__(256) unsigned char
+    g_noalloc_scratch[256 + (kNoAllocWedgeEntries + kNoAllocTailEntries) * sizeof(uint32_t)];
 
 // Device address of g_noalloc_scratch per device (host code cannot use the
 // symbol itself: on the host it names a stand-in, not device memory).
@@ -440,26 +518,14 @@ cudaError_t launch_normal_f64_noalloc(uint32_t seed, uint32_t first, uint32_t n,
         scratch = static_cast<unsigned char *>(addr);
         g_noalloc_addr[dev].store(scratch);
     }
-    unsigned long long *count = reinterpret_cast<unsigned long long *>(scratch);
-    uint32_t *list = reinterpret_cast<uint32_t *>(scratch + 256);
-    const size_t want = default_capacity(n);
-    const unsigned long long capacity =
-        static_cast<unsigned long long>(want < kNoAllocListEntries ? want : kNoAllocListEntries);
-
-    if ((err = cudaMemsetAsync(count, 0, sizeof(unsigned long long), s)) != cudaSuccess) return err;
-    const uint32_t key = seed_key(seed);
-    const uint32_t head = head_elems<double>(out, n);
-    const uint32_t n_vec = (n - head) / 2u;
-    const uint32_t blocks = n_vec ? (n_vec + kTableVecPerBlock - 1u) / kTableVecPerBlock : 1u;
-    zig_table_pass<<<blocks, kTableThreads, 0, s>>>(key, first, out, head, n_vec, n, list, count, capacity);
-    note_launch();
-    const uint32_t max_blocks = g_noalloc_sms[dev].load() * 4u;
-    const uint32_t want_blocks = (n + 8191u) / 8192u;
-    const uint32_t miss_blocks = want_blocks < 1u ? 1u : (want_blocks > max_blocks ? max_blocks : want_blocks);
-    zig_miss_pass<<<miss_blocks, kMissThreads, 0, s>>>(key, purpose_key(seed, kPurposeNormal64), first, out, n,
-                                                       list, count, capacity);
-    note_launch();
-    return cudaGetLastError();
+    MissList ml;
+    ml.counts = reinterpret_cast<unsigned long long *>(scratch);
+    ml.wedge = reinterpret_cast<uint32_t *>(scratch + 256);
+    ml.tail = ml.wedge + kNoAllocWedgeEntries;
+    const size_t want_w = wedge_capacity(n), want_t = tail_capacity(n);
+    ml.wedge_cap = static_cast<unsigned long long>(want_w < kNoAllocWedgeEntries ? want_w : kNoAllocWedgeEntries);
+    ml.tail_cap = static_cast<unsigned long long>(want_t < kNoAllocTailEntries ? want_t : kNoAllocTailEntries);
+    return enqueue_ziggurat(seed, first, n, out, ml, g_noalloc_sms[dev].load(), s);
 }
 
 }  // namespace rngk
