@@ -11,7 +11,8 @@
 //   small and an absolutely accurate log is not enough), otherwise
 //   ln 2 * log2(1 - u0) from the hardware log2 (absolute error <= 2^-22 on
 //   [1/2, 1], i.e. radius error <= 7e-7 for radii >= 1/4);
-//   radius = t * rsqrt(t), t = -2L (0 when u0 = 0);
+//   radius = sqrt(t), t = -2L, from the hardware square root (t is 0 or at
+//   least 2^-22, never subnormal, so the flush-to-zero forms lose nothing);
 //   cos(2 pi u1) = -cos(2 pi (u1 - 1/2)) with u1 - 1/2 = (1 + u1) - 3/2 exact,
 //   so the hardware cosine runs on [-pi, pi), where its absolute error is
 //   below 2^-21.4 (tandem-sycl "Design", section Normals: the angle shifted
@@ -22,6 +23,29 @@
 
 namespace rngk {
 namespace {
+
+// Hardware approximations (PTX .approx, flush-to-zero: no operand here is
+// subnormal).
+__device__ __forceinline__ float lg2_approx(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float sqrt_approx(float x)
+{
+    float y;
+    asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float cos_approx(float x)
+{
+    float y;
+    asm("cos.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 struct GenNormalF32 {
     using T = float;
@@ -36,12 +60,11 @@ struct GenNormalF32 {
         series = __fmaf_rn(u0, series, 0.333333343f);
         series = __fmaf_rn(u0, series, 0.5f);
         series = __fmaf_rn(u0, series, 1.0f);
-        const float minus_two_l_small = 2.0f * u0 * series;               // -2 ln(1 - u0), u0 small
-        const float minus_two_l_large = -1.38629436f * __log2f(v);         // -2 ln 2 log2(1 - u0)
+        const float minus_two_l_small = (2.0f * u0) * series;         // -2 ln(1 - u0), u0 small
+        const float minus_two_l_large = -1.38629436f * lg2_approx(v);  // -2 ln 2 log2(1 - u0)
         const float t = (h.hi & 0x7C0000u) ? minus_two_l_large : minus_two_l_small;  // u0 >= 2^-5 ?
-        const float radius = t > 0.0f ? t * rsqrtf(t) : 0.0f;
         const float u1_minus_half = __uint_as_float(0x3F800000u | (h.lo & 0x7FFFFFu)) - 1.5f;
-        return -radius * __cosf(u1_minus_half * 6.28318530717958647692f);
+        return -sqrt_approx(t) * cos_approx(u1_minus_half * 6.28318530717958647692f);
     }
 };
 

@@ -55,11 +55,21 @@ __device__ const double kZigX[kLayers + 1] = {ZIG_X_VALUES};
 __device__ const double2 kZigHalfXNext[kLayers] = {ZIG_HALFX_XNEXT_VALUES};  // {X[j]/2, X[j+1]}
 __device__ const double2 kZigFHalfDiff[kLayers] = {ZIG_F_HALFDIFF_VALUES};   // {F[j], (F[j+1]-F[j])/2}
 
-constexpr uint32_t kTableThreads = 256;
-constexpr uint32_t kTableIters = 8;  // 16-byte vectors per thread and block
-constexpr uint32_t kTableVecPerBlock = kTableThreads * kTableIters;  // 4096 elements
-constexpr uint32_t kWedgeQueue = 1024;  // per-block queues (17.5 and 0.23 misses expected)
-constexpr uint32_t kTailQueue = 64;
+// Table pass: one persistent block of 1024 threads per SM.  The block keeps
+// kTableCopies copies of the {X[j]/2, X[j+1]} table in shared memory, copy q
+// in 16-byte bank group q (entry j of copy q at index 8j + q); lane l reads
+// copy l mod 8, so the eight lanes of each quarter-warp phase of a 16-byte
+// gather hit eight different bank groups whatever their layers: 4 wavefronts
+// per warp instead of one per distinct cache line from L1.
+constexpr uint32_t kTableThreads = 1024;
+constexpr uint32_t kTableCopies = 8;
+constexpr uint32_t kTableWarps = kTableThreads / 32u;
+// Each warp queues its misses (element index, bit 31 set for a base-layer
+// miss) in shared memory and flushes them 32 at a time with one atomic per
+// list; two pushes of up to 32 entries can follow a flush check.
+constexpr uint32_t kWarpQueue = 96;
+constexpr size_t kTableSmem =
+    kLayers * kTableCopies * sizeof(double2) + kTableWarps * kWarpQueue * sizeof(uint32_t);
 constexpr uint32_t kMissThreads = 128;
 constexpr uint32_t kMissBlocksPerSm = 8;
 constexpr uint32_t kMaxRounds = 4096;  // rejection rounds of one miss (never reached)
@@ -222,60 +232,104 @@ __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint3
 
 // ---- kernels -----------------------------------------------------------------
 
-// warp-aggregated append of the lanes in `ballot` (this lane if `mine`) to a
-// shared queue
-__device__ __forceinline__ void queue_append(uint32_t ballot, bool mine, uint32_t e, uint32_t *queue,
-                                             uint32_t *queued, uint32_t capacity)
+// Flush the first `cnt` (<= 32) entries of a warp's queue to the global
+// lists (one atomic per list), then move the rest of the queue down.
+__device__ __forceinline__ void warp_queue_flush(uint32_t *q, uint32_t &qn, uint32_t cnt, const MissList &ml)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    uint32_t slot0 = 0;
-    if (lane == 0) slot0 = atomicAdd(queued, static_cast<uint32_t>(__popc(ballot)));
-    slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
-    if (mine) {
-        const uint32_t slot = slot0 + __popc(ballot & ((1u << lane) - 1u));
-        if (slot < capacity) queue[slot] = e;
+    const uint32_t below = (1u << lane) - 1u;
+    __syncwarp();
+    const bool have = lane < cnt;
+    const uint32_t e = have ? q[lane] : 0u;
+    const bool tail = have && (e >> 31);
+    const uint32_t tails = __ballot_sync(0xFFFFFFFFu, tail);
+    const uint32_t wedges = __ballot_sync(0xFFFFFFFFu, have && !tail);
+    unsigned long long wbase = 0, tbase = 0;
+    if (lane == 0) {
+        if (wedges) wbase = atomicAdd(&ml.counts[0], static_cast<unsigned long long>(__popc(wedges)));
+        if (tails) tbase = atomicAdd(&ml.counts[1], static_cast<unsigned long long>(__popc(tails)));
     }
+    wbase = __shfl_sync(0xFFFFFFFFu, wbase, 0);
+    tbase = __shfl_sync(0xFFFFFFFFu, tbase, 0);
+    if (tail) {
+        const unsigned long long slot = tbase + __popc(tails & below);
+        if (slot < ml.tail_cap) ml.tail[slot] = e & 0x7FFFFFFFu;
+    } else if (have) {
+        const unsigned long long slot = wbase + __popc(wedges & below);
+        if (slot < ml.wedge_cap) ml.wedge[slot] = e;
+    }
+    const uint32_t rest = qn - cnt;
+    const uint32_t r0 = lane < rest ? q[cnt + lane] : 0u;
+    const uint32_t r1 = lane + 32u < rest ? q[cnt + 32u + lane] : 0u;
+    __syncwarp();
+    if (lane < rest) q[lane] = r0;
+    if (lane + 32u < rest) q[32u + lane] = r1;
+    __syncwarp();
+    qn = rest;
 }
 
-__global__ void __launch_bounds__(kTableThreads)
+// Fast path with the layer table in shared memory (this lane's copy).
+__device__ __forceinline__ FastDraw zig_fast_shared(Words w, const double2 *my_copy)
+{
+    const uint32_t j = w.lo & (kLayers - 1u);
+    const double2 e = my_copy[j * kTableCopies];
+    const uint64_t xb = static_cast<uint64_t>(__double_as_longlong(scaled_by_u53(w, e.x)));
+    FastDraw d;
+    d.fast = xb < static_cast<uint64_t>(__double_as_longlong(e.y));
+    d.bits = xb | (static_cast<uint64_t>(w.lo & 0x400u) << 53);  // bit 10 -> sign bit
+    d.base = j == 0;
+    return d;
+}
+
+__global__ void __launch_bounds__(kTableThreads, 1)
 zig_table_pass(uint32_t key, uint32_t first, double *__restrict__ out, uint32_t head, uint32_t n_vec, uint32_t n,
                MissList ml)
 {
-    __shared__ uint32_t wedge_q[kWedgeQueue];
-    __shared__ uint32_t tail_q[kTailQueue];
-    __shared__ uint32_t wedge_n, tail_n;
-    __shared__ unsigned long long wedge_base, tail_base;
-    if (threadIdx.x == 0) wedge_n = tail_n = 0;
+    extern __shared__ __align__(16) unsigned char smem[];
+    double2 *table = reinterpret_cast<double2 *>(smem);
+    uint32_t *queues = reinterpret_cast<uint32_t *>(smem + kLayers * kTableCopies * sizeof(double2));
+    for (uint32_t i = threadIdx.x; i < kLayers * kTableCopies; i += kTableThreads)
+        table[i] = __ldg(&kZigHalfXNext[i / kTableCopies]);
     __syncthreads();
 
-    auto push = [&](const FastDraw &d, bool valid, uint32_t e) {
-        const bool miss = valid && !d.fast;
-        const uint32_t any = __ballot_sync(0xFFFFFFFFu, miss);
-        if (any) {
-            const bool tail = miss && d.base;
-            const uint32_t tails = __ballot_sync(0xFFFFFFFFu, tail);
-            queue_append(any & ~tails, miss && !tail, e, wedge_q, &wedge_n, kWedgeQueue);
-            if (tails) queue_append(tails, tail, e, tail_q, &tail_n, kTailQueue);
-        }
-    };
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t below = (1u << lane) - 1u;
+    uint32_t *q = queues + (threadIdx.x >> 5) * kWarpQueue;
+    uint32_t qn = 0;  // warp-uniform
+    const double2 *my_copy = table + (lane & (kTableCopies - 1u));
 
-    const uint32_t v_begin = blockIdx.x * kTableVecPerBlock;
-#pragma unroll 2
-    for (uint32_t it = 0; it < kTableIters; ++it) {
-        const uint32_t v = v_begin + it * kTableThreads + threadIdx.x;
+    auto push = [&](const FastDraw &d, bool miss, uint32_t e) {
+        const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, miss);
+        if (miss) q[qn + __popc(ballot & below)] = e | (static_cast<uint32_t>(d.base) << 31);
+        qn += __popc(ballot);
+    };
+    // one 16-byte vector (two elements) per lane; misses are rare (a warp
+    // step of 64 elements has one with probability 0.24), so the queue is
+    // touched only when the warp's ballot finds one
+    auto step = [&](uint32_t v, bool valid) {
         const uint32_t e0 = head + 2u * v;
-        const bool valid = v < n_vec;
         FastDraw a{}, b{};
         if (valid) {
-            a = zig_fast(draw64_words(key, first + e0));
-            b = zig_fast(draw64_words(key, first + e0 + 1u));
+            a = zig_fast_shared(draw64_words(key, first + e0), my_copy);
+            b = zig_fast_shared(draw64_words(key, first + e0 + 1u), my_copy);
             const uint4 u = make_uint4(static_cast<uint32_t>(a.bits), static_cast<uint32_t>(a.bits >> 32),
                                        static_cast<uint32_t>(b.bits), static_cast<uint32_t>(b.bits >> 32));
             __stcs(reinterpret_cast<uint4 *>(out + e0), u);
         }
-        push(a, valid, e0);
-        push(b, valid, e0 + 1u);
-    }
+        const bool m0 = valid && !a.fast, m1 = valid && !b.fast;
+        if (__any_sync(0xFFFFFFFFu, m0 || m1)) {
+            push(a, m0, e0);
+            push(b, m1, e0 + 1u);
+            while (qn >= 32u) warp_queue_flush(q, qn, 32u, ml);
+        }
+    };
+
+    // warp-uniform stride over 16-byte vectors: each warp stores 512
+    // contiguous bytes per step; whole warps first, then the ragged end
+    const uint32_t stride = gridDim.x * kTableThreads;
+    uint32_t vb = blockIdx.x * kTableThreads + (threadIdx.x & ~31u);
+    for (; vb + 32u <= n_vec; vb += stride) step(vb + lane, true);
+    for (; vb < n_vec; vb += stride) step(vb + lane, vb + lane < n_vec);
     // the peeled head and tail (at most one element each), by warp 0 of block 0
     if (blockIdx.x == 0 && threadIdx.x < 32u) {
         const uint32_t tail0 = head + 2u * n_vec;
@@ -290,29 +344,13 @@ zig_table_pass(uint32_t key, uint32_t first, double *__restrict__ out, uint32_t 
         }
         FastDraw d{};
         if (here) {
-            d = zig_fast(draw64_words(key, first + e));
+            d = zig_fast_shared(draw64_words(key, first + e), my_copy);
             out[e] = __longlong_as_double(static_cast<long long>(d.bits));
         }
-        push(d, here, e);
+        push(d, here && !d.fast, e);
+        while (qn >= 32u) warp_queue_flush(q, qn, 32u, ml);
     }
-    __syncthreads();
-    const uint32_t nw = wedge_n, nt = tail_n;
-    if (nw == 0 && nt == 0) return;
-    // one atomic per list and block; a full queue forces the count past the
-    // capacity, which sends the miss pass through the whole-fill walk
-    if (threadIdx.x == 0) {
-        if (nw) wedge_base = atomicAdd(&ml.counts[0], nw <= kWedgeQueue ? nw : ml.wedge_cap + 1ull);
-        if (nt) tail_base = atomicAdd(&ml.counts[1], nt <= kTailQueue ? nt : ml.tail_cap + 1ull);
-    }
-    __syncthreads();
-    if (nw && nw <= kWedgeQueue) {
-        for (uint32_t i = threadIdx.x; i < nw; i += kTableThreads)
-            if (wedge_base + i < ml.wedge_cap) ml.wedge[wedge_base + i] = wedge_q[i];
-    }
-    if (nt && nt <= kTailQueue) {
-        for (uint32_t i = threadIdx.x; i < nt; i += kTableThreads)
-            if (tail_base + i < ml.tail_cap) ml.tail[tail_base + i] = tail_q[i];
-    }
+    if (qn) warp_queue_flush(q, qn, qn, ml);
 }
 
 __global__ void __launch_bounds__(kMissThreads)
@@ -358,6 +396,9 @@ size_t tail_capacity(uint32_t n)
     return static_cast<size_t>(mean + 16.0 * std::sqrt(mean + 1.0) + 1024.0);
 }
 
+constexpr int kMaxDevices = 64;
+std::atomic<bool> g_table_smem_set[kMaxDevices];  // dynamic shared memory limit raised on the device
+
 // Table pass + miss pass of one piece into the lists of `ml` (counts cleared
 // here first).
 cudaError_t enqueue_ziggurat(uint32_t seed, uint32_t first, uint32_t n, double *out, const MissList &ml,
@@ -365,11 +406,21 @@ cudaError_t enqueue_ziggurat(uint32_t seed, uint32_t first, uint32_t n, double *
 {
     cudaError_t err = cudaMemsetAsync(ml.counts, 0, 2 * sizeof(unsigned long long), s);
     if (err != cudaSuccess) return err;
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_table_smem_set[dev].load()) {
+        err = cudaFuncSetAttribute(zig_table_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kTableSmem));
+        if (err != cudaSuccess) return err;
+        g_table_smem_set[dev].store(true);
+    }
     const uint32_t key = seed_key(seed);
     const uint32_t head = head_elems<double>(out, n);
     const uint32_t n_vec = (n - head) / 2u;
-    const uint32_t blocks = n_vec ? (n_vec + kTableVecPerBlock - 1u) / kTableVecPerBlock : 1u;
-    zig_table_pass<<<blocks, kTableThreads, 0, s>>>(key, first, out, head, n_vec, n, ml);
+    const uint32_t want = (n_vec + kTableThreads - 1u) / kTableThreads;
+    const uint32_t blocks = want < 1u ? 1u : (want < sms ? want : sms);
+    zig_table_pass<<<blocks, kTableThreads, kTableSmem, s>>>(key, first, out, head, n_vec, n, ml);
     note_launch();
     const uint32_t max_blocks = sms * kMissBlocksPerSm;
     const uint32_t want_blocks = (n + 4095u) / 4096u;
@@ -489,7 +540,7 @@ namespace {
 
 constexpr size_t kNoAllocTailEntries = size_t(1) << 16;
 constexpr size_t kNoAllocWedgeEntries = (size_t(1) << 21) - kNoAllocTailEntries;
-constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocMaxDevices = kMaxDevices;
 
 static __device__ __align__(256) unsigned char
     g_noalloc_scratch[256 + (kNoAllocWedgeEntries + kNoAllocTailEntries) * sizeof(uint32_t)];
