@@ -36,6 +36,20 @@ __device__ __forceinline__ void store16(T *p, const Vec16<T> &x)
     __stcs(reinterpret_cast<uint4 *>(p), u);
 }
 
+// Vectors a thread computes per loop step: a generator may declare
+// `static constexpr uint32_t kVectorsPerStep = 2` to keep twice the
+// independent hash chains in flight (the bounded and 64-bit fills, whose
+// multiplies have long latencies); the plain draws stay at one, which keeps
+// each warp's stores of one step in consecutive lines.
+template <class Gen, class = void>
+struct VectorsPerStep {
+    static constexpr uint32_t value = 1;
+};
+template <class Gen>
+struct VectorsPerStep<Gen, decltype(void(Gen::kVectorsPerStep))> {
+    static constexpr uint32_t value = Gen::kVectorsPerStep;
+};
+
 template <class Gen>
 __global__ void __launch_bounds__(kFillThreads)
 fill_kernel(Gen gen, typename Gen::T *__restrict__ out, uint32_t first, uint32_t head, uint32_t n_vec,
@@ -52,7 +66,21 @@ fill_kernel(Gen gen, typename Gen::T *__restrict__ out, uint32_t first, uint32_t
 
     T *body = out + head;
     const uint32_t c0 = first + head;
-    for (uint32_t v = tid; v < n_vec; v += stride) {
+    uint32_t v = tid;
+    if (VectorsPerStep<Gen>::value == 2) {
+        for (; v + stride < n_vec; v += 2u * stride) {
+            Vec16<T> x, y;
+            const uint32_t cx = c0 + v * kPer, cy = c0 + (v + stride) * kPer;
+#pragma unroll
+            for (uint32_t k = 0; k < kPer; ++k) {
+                x.v[k] = gen(cx + k);
+                y.v[k] = gen(cy + k);
+            }
+            store16(body + v * kPer, x);
+            store16(body + (v + stride) * kPer, y);
+        }
+    }
+    for (; v < n_vec; v += stride) {
         Vec16<T> x;
         const uint32_t c = c0 + v * kPer;
 #pragma unroll

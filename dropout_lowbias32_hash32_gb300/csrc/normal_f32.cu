@@ -49,6 +49,7 @@ __device__ __forceinline__ float cos_approx(float x)
 
 struct GenNormalF32 {
     using T = float;
+    static constexpr uint32_t kVectorsPerStep = 2;
     uint32_t key;  // folded hash of the seed
     __device__ T operator()(uint32_t c) const
     {
