@@ -7,29 +7,30 @@ The outputs (1-2 GiB each) are far larger than the 129 MB L2, so no flush is
 needed between timed steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--only FILL[,FILL...]] [--n ELEMENTS] [--no-e2e] [--no-cpu]
 
 Prints one JSON line (rank 0).  `value` is the bytes all fills wrote per
-step over the step time (GiB/s, max over ranks), the `fills` table breaks it
-down per fill, `roofline` relates the slowest kernel to the measured HBM
-bandwidth, `e2e` repeats the step through the same C ABI with pinned host
-buffers (inputs copied in, every output copied out, inside the timed
-region), `cpu_baseline` times the CPU oracle on a bounded sample.  Under
-torchrun each rank fills its own counter range (weak scaling, no data
-exchange).  --impl reference times the CPU oracle itself as the reference
-arm.
+step over the step time (GiB/s, max over ranks); `fills` breaks it down per
+fill (CUDA events around each call on its stream); `roofline` relates the
+kernel with the largest share of the step to the measured HBM bandwidth and
+`slowest_fill` gives the slowest call with the pipe that bounds it; `e2e`
+repeats the step through the same C ABI with pinned host buffers (inputs
+copied in, every output copied out, inside the timed region);
+`cpu_baseline` times the CPU oracle on a bounded sample.  Under torchrun
+each rank fills its own counter range (weak scaling, no data exchange).
+--impl reference times the CPU oracle itself as the reference arm.
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
+import hashlib
 import json
-import math
 import os
 import statistics
-import subprocess
 import sys
+import threading
 import time
-
-import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -44,107 +45,171 @@ WORKLOAD = ("every fill at 2^28 elements per step: u32/u64/f32/f64 (seed 0x9E377
             "cycling 0, 1, 3, 2^32-5), u32_below(1000|2^32-2), u64_below(1000|2^64-2), i32/i64 "
             "low+below32(1000) and i64 low+below64(1000) (low -500, seeds 1..4), normal_f32 and "
             "normal_f64 (seed 7), dropout fwd+bwd on X[2^20,256] at p=0.1 and 0.5 (seed 42)")
+CSRC = os.path.join(ROOT, "dropout_lowbias32_hash32_gb300", "csrc")
 
 
 # ---------------------------------------------------------------- the step --
+class Fill:
+    """One call of the step: output buffer kind, bytes written and read per
+    element, the kernel it launches and its source file, and the call."""
+
+    def __init__(self, name, kind, written, read, kernel, source, call):
+        self.name, self.kind, self.written, self.read = name, kind, written, read
+        self.kernel, self.source, self.call = kernel, source, call
+
+
 def fill_specs():
-    """(name, dtype, bytes per element written, bytes read, call(rng, out, first, x, y))."""
     b32, b64 = (1 << 32) - 2, (1 << 64) - 2
+    F = Fill
     return [
-        ("u32", "int32", 4, 0, lambda r, o, f, s: r.rng_fill_u32(W.UNIFORM_SEED, f, o, s)),
-        ("u64", "int64", 8, 0, lambda r, o, f, s: r.rng_fill_u64(W.UNIFORM_SEED, f, o, s)),
-        ("f32", "float32", 4, 0, lambda r, o, f, s: r.rng_fill_f32(W.UNIFORM_SEED, f, o, s)),
-        ("f64", "float64", 8, 0, lambda r, o, f, s: r.rng_fill_f64(W.UNIFORM_SEED, f, o, s)),
-        ("u32_below_1000", "int32", 4, 0, lambda r, o, f, s: r.rng_fill_u32_below(1, f, 1000, o, s)),
-        ("u32_below_2^32-2", "int32", 4, 0, lambda r, o, f, s: r.rng_fill_u32_below(2, f, b32, o, s)),
-        ("u64_below_1000", "int64", 8, 0, lambda r, o, f, s: r.rng_fill_u64_below(3, f, 1000, o, s)),
-        ("u64_below_2^64-2", "int64", 8, 0, lambda r, o, f, s: r.rng_fill_u64_below(4, f, b64, o, s)),
-        ("i32_range", "int32", 4, 0, lambda r, o, f, s: r.rng_fill_i32_range(1, f, W.LOW, 1000, o, s)),
-        ("i64_range32", "int64", 8, 0, lambda r, o, f, s: r.rng_fill_i64_range32(2, f, W.LOW, 1000, o, s)),
-        ("i64_range", "int64", 8, 0, lambda r, o, f, s: r.rng_fill_i64_range(3, f, W.LOW, 1000, o, s)),
-        ("normal_f32", "float32", 4, 0, lambda r, o, f, s: r.rng_fill_normal_f32(W.NORMAL_SEED, f, o, s)),
-        ("normal_f64", "float64", 8, 0, lambda r, o, f, s: r.rng_fill_normal_f64(W.NORMAL_SEED, f, o, s)),
-        ("dropout_fwd_p0.1", "x", 4, 4, lambda r, o, f, s: r.rng_dropout_fwd(o[0], o[1], 0.1, W.DROPOUT_SEED, f, s)),
-        ("dropout_bwd_p0.1", "dy", 4, 4, lambda r, o, f, s: r.rng_dropout_bwd(o[0], o[1], 0.1, W.DROPOUT_SEED, f, s)),
-        ("dropout_fwd_p0.5", "x", 4, 4, lambda r, o, f, s: r.rng_dropout_fwd(o[0], o[1], 0.5, W.DROPOUT_SEED, f, s)),
-        ("dropout_bwd_p0.5", "dy", 4, 4, lambda r, o, f, s: r.rng_dropout_bwd(o[0], o[1], 0.5, W.DROPOUT_SEED, f, s)),
+        F("u32", "int32", 4, 0, "fill_kernel<GenU32>", "fill_uniform.cu",
+          lambda r, o, f, s: r.rng_fill_u32(W.UNIFORM_SEED, f, o, s)),
+        F("u64", "int64", 8, 0, "fill_kernel<GenU64>", "fill_uniform.cu",
+          lambda r, o, f, s: r.rng_fill_u64(W.UNIFORM_SEED, f, o, s)),
+        F("f32", "float32", 4, 0, "fill_kernel<GenF32>", "fill_uniform.cu",
+          lambda r, o, f, s: r.rng_fill_f32(W.UNIFORM_SEED, f, o, s)),
+        F("f64", "float64", 8, 0, "fill_kernel<GenF64>", "fill_uniform.cu",
+          lambda r, o, f, s: r.rng_fill_f64(W.UNIFORM_SEED, f, o, s)),
+        F("u32_below_1000", "int32", 4, 0, "fill_kernel<GenBelow32>", "fill_bounded.cu",
+          lambda r, o, f, s: r.rng_fill_u32_below(1, f, 1000, o, s)),
+        F("u32_below_2^32-2", "int32", 4, 0, "fill_kernel<GenBelow32>", "fill_bounded.cu",
+          lambda r, o, f, s: r.rng_fill_u32_below(2, f, b32, o, s)),
+        F("u64_below_1000", "int64", 8, 0, "fill_kernel<GenBelow64>", "fill_bounded.cu",
+          lambda r, o, f, s: r.rng_fill_u64_below(3, f, 1000, o, s)),
+        F("u64_below_2^64-2", "int64", 8, 0, "fill_kernel<GenBelow64>", "fill_bounded.cu",
+          lambda r, o, f, s: r.rng_fill_u64_below(4, f, b64, o, s)),
+        F("i32_range", "int32", 4, 0, "fill_kernel<GenI32Range>", "fill_bounded.cu",
+          lambda r, o, f, s: r.rng_fill_i32_range(1, f, W.LOW, 1000, o, s)),
+        F("i64_range32", "int64", 8, 0, "fill_kernel<GenI64Range32>", "fill_bounded.cu",
+          lambda r, o, f, s: r.rng_fill_i64_range32(2, f, W.LOW, 1000, o, s)),
+        F("i64_range", "int64", 8, 0, "fill_kernel<GenI64Range>", "fill_bounded.cu",
+          lambda r, o, f, s: r.rng_fill_i64_range(3, f, W.LOW, 1000, o, s)),
+        F("normal_f32", "float32", 4, 0, "fill_kernel<GenNormalF32>", "normal_f32.cu",
+          lambda r, o, f, s: r.rng_fill_normal_f32(W.NORMAL_SEED, f, o, s)),
+        F("normal_f64", "float64", 8, 0, "zig_table_pass+zig_miss_pass", "normal_f64.cu",
+          lambda r, o, f, s: r.rng_fill_normal_f64(W.NORMAL_SEED, f, o, s)),
+        F("dropout_fwd_p0.1", "x", 4, 4, "dropout_vec_kernel", "dropout.cu",
+          lambda r, o, f, s: r.rng_dropout_fwd(o[0], o[1], 0.1, W.DROPOUT_SEED, f, s)),
+        F("dropout_bwd_p0.1", "dy", 4, 4, "dropout_vec_kernel", "dropout.cu",
+          lambda r, o, f, s: r.rng_dropout_bwd(o[0], o[1], 0.1, W.DROPOUT_SEED, f, s)),
+        F("dropout_fwd_p0.5", "x", 4, 4, "dropout_vec_kernel", "dropout.cu",
+          lambda r, o, f, s: r.rng_dropout_fwd(o[0], o[1], 0.5, W.DROPOUT_SEED, f, s)),
+        F("dropout_bwd_p0.5", "dy", 4, 4, "dropout_vec_kernel", "dropout.cu",
+          lambda r, o, f, s: r.rng_dropout_bwd(o[0], o[1], 0.5, W.DROPOUT_SEED, f, s)),
     ]
 
 
-# Kernels each call launches and the kernel that dominates its time.
-KERNELS_PER_CALL = {"normal_f64": 2}
-
-
-def bytes_written_per_step(n: int) -> int:
-    return sum(n * w for _, _, w, _, _ in fill_specs())
+def selected_specs(only: str | None):
+    specs = fill_specs()
+    if not only:
+        return specs
+    want = only.split(",")
+    unknown = set(want) - {s.name for s in specs}
+    if unknown:
+        raise SystemExit(f"unknown fills: {sorted(unknown)}")
+    return [s for s in specs if s.name in want]
 
 
 # ------------------------------------------------------------------ peaks --
-def measured_peak_hbm():
+def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as fh:
-            return float(json.load(fh)["hbm_gbs"]), "measured"
-    except (OSError, KeyError, ValueError):
-        return 6800.0, "fallback"
+            return json.load(fh), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+def source_digest(source: str) -> str:
+    """sha256 over a kernel's own source file and the headers every kernel uses."""
+    h = hashlib.sha256()
+    for name in (source, "hash32.cuh", "fill_kernel.cuh", "internal.h", "zig_tables.inc"):
+        with open(os.path.join(CSRC, name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, source: str):
+    """DRAM bytes per element of `kernel` from profiles/dram_traffic.txt (an
+    ncu capture of dram__bytes_read.sum + dram__bytes_write.sum), or None if
+    there is none or the kernel's sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    digest = source_digest(source)
+    for line in lines:
+        f = line.split()
+        if len(f) >= 5 and f[0] == kernel and not line.startswith("#"):
+            elements, read, write, dig = int(f[1]), int(f[2]), int(f[3]), f[4]
+            if dig == digest:
+                return (read + write) / elements
+    return None
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """SM clock, power and clock-event reasons sampled every 5 ms through NVML
+    while the timed region runs (read-only queries)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+    def __init__(self, uuid: str | None, period: float = 0.005):
+        self.period, self.samples, self.max_mhz = period, [], None
+        self.stop = threading.Event()
+        self.thread = None
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            handle = ctypes.c_void_p()
+            if uuid is None or nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) != 0:
+                raise OSError("no NVML handle for this device")
+            self.nvml, self.handle = nvml, handle
+            mx = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.error = None
+        except OSError as exc:
+            self.nvml, self.error = None, str(exc)
+
+    def _run(self):
+        clk, mw, reasons = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop.is_set():
+            ok = self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0
+            self.nvml.nvmlDeviceGetPowerUsage(self.handle, ctypes.byref(mw))
+            get_reasons(self.handle, ctypes.byref(reasons))
+            if ok:
+                self.samples.append((clk.value, mw.value / 1000.0, reasons.value))
+            self.stop.wait(self.period)
 
     def __enter__(self):
-        try:
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.fh.close()
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join()
 
     def summary(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        with open(self.path) as fh:
-            for line in fh:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [self.error or "no samples"]}
+        reasons = sorted({name for _, _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples),
+                "power_w_max": round(max(s[1] for s in self.samples), 1)}
 
 
 # ------------------------------------------------------------- CPU oracle --
-def oracle_sample(orc, n_sample: int, first: int):
-    """Run every fill of the step on n_sample elements with the oracle;
-    returns (seconds, bytes written) per fill."""
+def oracle_sample(orc, specs, n_sample: int, first: int):
+    """Run the step's fills on n_sample elements with the oracle; returns
+    {fill: (seconds, bytes written)}."""
     x = W.dropout_x(n_sample)
     dy = W.dropout_dy(n_sample)
     calls = {
@@ -167,29 +232,36 @@ def oracle_sample(orc, n_sample: int, first: int):
         "dropout_bwd_p0.5": lambda: orc.dropout(dy, 0.5, W.DROPOUT_SEED, first),
     }
     out = {}
-    for name, _, width, _, _ in fill_specs():
+    for spec in specs:
         t0 = time.perf_counter()
-        calls[name]()
-        out[name] = (time.perf_counter() - t0, n_sample * width)
+        calls[spec.name]()
+        out[spec.name] = (time.perf_counter() - t0, n_sample * spec.written)
     return out
 
 
-def cpu_baseline(n_sample: int = 1 << 26):
-    """The oracle, single-threaded, on n_sample elements of every fill: the
-    GiB/s it would write over a whole step (bytes / summed seconds)."""
+def cpu_baseline(specs, n_sample: int = 1 << 26):
+    """The oracle, single-threaded, on n_sample elements of every fill of the
+    step: the GiB/s it would write over a whole step (bytes / seconds)."""
     import oracle
     orc = oracle.default()
     orc.zig1024()  # builds its table outside the timing
-    res = oracle_sample(orc, n_sample, 0)
+    res = oracle_sample(orc, specs, n_sample, 0)
     secs = sum(t for t, _ in res.values())
     written = sum(b for _, b in res.values())
-    return {"value": written / secs / GIB, "unit": "GiB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(written / secs / GIB, 4), "unit": "GiB/s", "cores": 1, "kind": "oracle",
             "sample": f"every fill of the step on {n_sample} elements (counters 0..{n_sample - 1}), "
-                      f"single-threaded C oracle, {secs:.1f} s",
-            "seconds": secs}
+                      f"single-threaded C oracle, {secs:.1f} s"}
 
 
 # --------------------------------------------------------------- our arm ---
+def device_uuid(torch, dev):
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    if uuid is None:
+        return None
+    uuid = str(uuid)
+    return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+
+
 def run_ours(args):
     import torch
 
@@ -210,30 +282,28 @@ def run_ours(args):
 
     n = args.n
     dev = torch.device("cuda", local)
-    specs = fill_specs()
+    specs = selected_specs(args.only)
     buf4 = torch.empty(n, dtype=torch.int32, device=dev)
     buf8 = torch.empty(n, dtype=torch.int64, device=dev)
-    host_x = torch.from_numpy(W.dropout_x(n)).pin_memory()
-    host_dy = torch.from_numpy(W.dropout_dy(n)).pin_memory()
-    x = host_x.to(dev)
-    dy = host_dy.to(dev)
-    y = torch.empty_like(x)
+    needs_inputs = any(s.kind in ("x", "dy") for s in specs)
+    host_x = torch.from_numpy(W.dropout_x(n)).pin_memory() if needs_inputs else None
+    host_dy = torch.from_numpy(W.dropout_dy(n)).pin_memory() if needs_inputs else None
+    x = host_x.to(dev) if needs_inputs else None
+    dy = host_dy.to(dev) if needs_inputs else None
+    y = torch.empty(n, dtype=torch.float32, device=dev) if needs_inputs else None
     outs = {"int32": buf4, "float32": buf4.view(torch.float32), "int64": buf8,
             "float64": buf8.view(torch.float64), "x": (x, y), "dy": (dy, y)}
     stream = torch.cuda.current_stream(dev)
     # rank r fills elements [r n, (r + 1) n) of each global fill
     base = (rank * n) & 0xFFFFFFFF
 
-    def first_of(step):
-        return (W.FIRST_COUNTERS[step % len(W.FIRST_COUNTERS)] + base) & 0xFFFFFFFF
-
     def step(k, events=None):
-        f = first_of(k)
-        for i, (name, kind, _, _, call) in enumerate(specs):
-            first = f if name in ("u32", "u64", "f32", "f64") else base
+        cycled = (W.FIRST_COUNTERS[k % len(W.FIRST_COUNTERS)] + base) & 0xFFFFFFFF
+        for i, spec in enumerate(specs):
+            first = cycled if spec.name in ("u32", "u64", "f32", "f64") else base
             if events is not None:
                 events[i][0].record(stream)
-            call(rng, outs[kind], first, stream)
+            spec.call(rng, outs[spec.kind], first, stream)
             if events is not None:
                 events[i][1].record(stream)
 
@@ -241,12 +311,11 @@ def run_ours(args):
         step(k)
     torch.cuda.synchronize()
 
-    # per-fill events of every timed step
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in specs]
           for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = rng.rng_debug_launch_count()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(device_uuid(torch, dev)) as clocks:
         barrier()
         torch.cuda.synchronize()
         t_start.record(stream)
@@ -261,26 +330,50 @@ def run_ours(args):
         t = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    per_fill_ms = {name: statistics.median(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
-                   for i, (name, *_rest) in enumerate(specs)}
+    fill_ms = {spec.name: statistics.median(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
+               for i, spec in enumerate(specs)}
 
-    written = bytes_written_per_step(n)
+    written = sum(n * s.written for s in specs)
     value = written * world * args.steps / (elapsed_ms / 1e3) / GIB
-    peak, peak_kind = measured_peak_hbm()
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
     fills = {}
-    for name, _, width, read, _ in specs:
-        ms = per_fill_ms[name]
-        gbs = (width + read) * n / (ms / 1e3) / 1e9
-        fills[name] = {"ms": round(ms, 4), "gib_s_written": round(width * n / (ms / 1e3) / GIB, 1),
-                       "gb_s_traffic": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 3)}
-    dominant = max(specs, key=lambda s: per_fill_ms[s[0]])
-    dname, _, dwidth, dread, _ = dominant
-    dms = per_fill_ms[dname]
-    achieved = (dwidth + dread) * n / (dms / 1e3) / 1e9
+    for s in specs:
+        ms = fill_ms[s.name]
+        gbs = (s.written + s.read) * n / (ms / 1e3) / 1e9
+        fills[s.name] = {"ms": round(ms, 4), "gib_s_written": round(s.written * n / (ms / 1e3) / GIB, 1),
+                         "gb_s_traffic": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 3),
+                         "kernel": s.kernel}
+
+    # the kernel with the largest share of the step, over all of its calls
+    by_kernel = {}
+    for s in specs:
+        ms, nbytes, src = by_kernel.get(s.kernel, (0.0, 0, s.source))
+        by_kernel[s.kernel] = (ms + fill_ms[s.name], nbytes + (s.written + s.read) * n, src)
+    kname, (kms, kbytes, ksrc) = max(by_kernel.items(), key=lambda kv: kv[1][0])
+    calls = sum(1 for s in specs if s.kernel == kname)
+    achieved = kbytes / (kms / 1e3) / 1e9
+    per_elem = ncu_traffic(kname, ksrc)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 3), "traffic": None, "kernel": dname,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                else "fallback 6.8 TB/s"}
+                "frac": round(achieved / peak, 3),
+                "traffic": None if per_elem is None else int(per_elem * n),
+                "kernel": kname, "calls_per_step": calls,
+                "share_of_step": round(kms / sum(fill_ms.values()), 3),
+                "algorithmic_bytes_per_launch": kbytes // calls,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    slowest = max(specs, key=lambda s: fill_ms[s.name])
+    slow = {"fill": slowest.name, "kernel": slowest.kernel, "ms": fills[slowest.name]["ms"],
+            "frac_of_hbm": fills[slowest.name]["frac_of_hbm"]}
+    if slowest.name == "normal_f64":
+        # the fast path spends one DFMA per element; GB300 retires 2 DFMA per SM and cycle
+        props = torch.cuda.get_device_properties(dev)
+        mhz = clocks.summary().get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+        fp64_peak = 2.0 * props.multi_processor_count * mhz * 1e6
+        dfma = n / (fill_ms["normal_f64"] / 1e3)
+        slow.update({"bound": "fp64", "achieved": round(dfma / 1e9, 1), "peak": round(fp64_peak / 1e9, 1),
+                     "unit": "G DFMA/s (one per element on the fast path)", "frac": round(dfma / fp64_peak, 3)})
 
     e2e = None
     if not args.no_e2e:
@@ -295,11 +388,13 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
             "data": "synthetic (counter-based fills need no input; dropout X ~ U(-1,1), dY ~ N(0,1) f32 "
                     "from numpy PCG64 seeds 11, 12)",
-            "config": {"workload": WORKLOAD, "elements_per_fill": n, "fills_per_step": len(specs),
-                       "bytes_written_per_step": written, "l2": "outputs of 1-2 GiB per fill exceed "
-                       "the 129 MB L2; no flush between steps", "parallelism": f"counter-range shards x{world}"},
-            "fills": fills, "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clocks.summary(), "cpu_baseline": None if args.no_cpu else cpu_baseline(),
+            "config": {"workload": WORKLOAD if not args.only else f"{args.only} at {n} elements",
+                       "elements_per_fill": n, "fills_per_step": len(specs), "bytes_written_per_step": written,
+                       "l2": "outputs of 1-2 GiB per fill exceed the 129 MB L2; no flush between steps",
+                       "parallelism": f"counter-range shards x{world}"},
+            "fills": fills, "roofline": roofline, "slowest_fill": slow, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks.summary(),
+            "cpu_baseline": None if args.no_cpu else cpu_baseline(specs),
         }
         print(json.dumps(result), flush=True)
     if dist is not None:
@@ -318,20 +413,20 @@ def run_e2e(rng, torch, specs, outs, host_inputs, x, dy, n, stream, barrier, dis
     barrier()
     torch.cuda.synchronize()
     t0.record(stream)
-    for k in range(steps):
-        for name, kind, width, _, call in specs:
-            if kind in ("x", "dy"):
-                src, dst = (host_x, x) if kind == "x" else (host_dy, dy)
+    for _ in range(steps):
+        for spec in specs:
+            if spec.kind in ("x", "dy"):
+                src, dst = (host_x, x) if spec.kind == "x" else (host_dy, dy)
                 dst.copy_(src, non_blocking=True)
                 h2d += n * 4
-                target = outs[kind]
-                call(rng, target, 0, stream)
-                res = target[1]
+                spec.call(rng, outs[spec.kind], 0, stream)
+                res = outs[spec.kind][1]
             else:
-                res = outs[kind]
-                call(rng, res, 0, stream)
-            host_out[:n * width].copy_(res.view(torch.uint8).view(-1)[:n * width], non_blocking=True)
-            d2h += n * width
+                res = outs[spec.kind]
+                spec.call(rng, res, 0, stream)
+            nbytes = n * spec.written
+            host_out[:nbytes].copy_(res.view(torch.uint8).view(-1)[:nbytes], non_blocking=True)
+            d2h += nbytes
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -340,7 +435,7 @@ def run_e2e(rng, torch, specs, outs, host_inputs, x, dy, n, stream, barrier, dis
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    value = bytes_written_per_step(n) * world * steps / (ms / 1e3) / GIB
+    value = sum(n * s.written for s in specs) * world * steps / (ms / 1e3) / GIB
     return {"value": round(value, 1), "unit": "GiB/s", "h2d_bytes_per_step": h2d // steps,
             "d2h_bytes_per_step": d2h // steps, "steps": steps}
 
@@ -355,13 +450,14 @@ def run_reference(args):
     import oracle
     orc = oracle.default()
     orc.zig1024()
+    specs = selected_specs(args.only)
     n_sample = args.ref_sample
     for k in range(args.warmup):
-        oracle_sample(orc, max(n_sample // 16, 1024), k)
+        oracle_sample(orc, specs, max(n_sample // 16, 1024), k)
     t0 = time.perf_counter()
     written = 0
     for k in range(args.steps):
-        res = oracle_sample(orc, n_sample, W.FIRST_COUNTERS[k % 4])
+        res = oracle_sample(orc, specs, n_sample, W.FIRST_COUNTERS[k % 4])
         written += sum(b for _, b in res.values())
     secs = time.perf_counter() - t0
     value = written / secs / GIB
@@ -383,10 +479,11 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--n", type=int, default=N, help="elements per fill (default 2^28)")
+    ap.add_argument("--only", help="comma-separated fills of the step to run (default: all)")
     ap.add_argument("--ref-sample", type=int, default=1 << 20, help="oracle elements per fill and step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
