@@ -7,13 +7,15 @@ The outputs (1-2 GiB each) are far larger than the 129 MB L2, so no flush is
 needed between timed steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--only FILL[,FILL...]] [--n ELEMENTS] [--no-e2e] [--no-cpu]
+                    [--only FILL[,FILL...]] [--n ELEMENTS] [--no-e2e] [--no-cpu] [--no-next]
 
 Prints one JSON line (rank 0).  `value` is the bytes all fills wrote per
 step over the step time (GiB/s, max over ranks); `fills` breaks it down per
 fill (CUDA events around each call on its stream); `roofline` relates the
 kernel with the largest share of the step to the measured HBM bandwidth and
-`slowest_fill` gives the slowest call with the pipe that bounds it; `e2e`
+`slowest_fill` gives the slowest call with the pipe that bounds it;
+`next_rows` times the fills beyond the step (paired normals, narrow fills)
+one by one, outside `value`; `e2e`
 repeats the step through the same C ABI with pinned host buffers (inputs
 copied in, every output copied out, inside the timed region);
 `cpu_baseline` times the CPU oracle on a bounded sample.  Under torchrun
@@ -99,6 +101,23 @@ def fill_specs():
     ]
 
 
+def next_specs():
+    """Fills beyond the measured step (timed separately, not part of `value`)."""
+    F = Fill
+    return [
+        F("normal_f32_pairs", "float32", 4, 0, "fill_kernel<GenNormalF32Pairs>", "normal_f32.cu",
+          lambda r, o, f, s: r.rng_fill_normal_f32_pairs(W.NORMAL_SEED, f, o, s)),
+        F("u8", "uint8", 1, 0, "fill_kernel<GenU8>", "fill_narrow.cu",
+          lambda r, o, f, s: r.rng_fill_u8(W.UNIFORM_SEED, f, o, s)),
+        F("u16", "int16", 2, 0, "fill_kernel<GenU16>", "fill_narrow.cu",
+          lambda r, o, f, s: r.rng_fill_u16(W.UNIFORM_SEED, f, o, s)),
+        F("f16", "float16", 2, 0, "fill_kernel<GenF16>", "fill_narrow.cu",
+          lambda r, o, f, s: r.rng_fill_f16(W.UNIFORM_SEED, f, o, s)),
+        F("bool", "bool", 1, 0, "fill_kernel<GenBool>", "fill_narrow.cu",
+          lambda r, o, f, s: r.rng_fill_bool(W.UNIFORM_SEED, f, o, s)),
+    ]
+
+
 def selected_specs(only: str | None):
     specs = fill_specs()
     if not only:
@@ -123,8 +142,11 @@ def measured_peaks():
 def source_digest(source: str) -> str:
     """sha256 over a kernel's own source file and the headers every kernel uses."""
     h = hashlib.sha256()
-    for name in (source, "hash32.cuh", "fill_kernel.cuh", "internal.h", "zig_tables.inc"):
-        with open(os.path.join(CSRC, name), "rb") as fh:
+    paths = [os.path.join(CSRC, name) for name in (source, "hash32.cuh", "fill_kernel.cuh", "internal.h",
+                                                     "zig_tables.inc")]
+    paths.append(os.path.join(ROOT, "include", "rng_device.cuh"))
+    for path in paths:
+        with open(path, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -375,6 +397,27 @@ def run_ours(args):
         slow.update({"bound": "fp64", "achieved": round(dfma / 1e9, 1), "peak": round(fp64_peak / 1e9, 1),
                      "unit": "G DFMA/s (one per element on the fast path)", "frac": round(dfma / fp64_peak, 3)})
 
+    next_rows = None
+    if not args.no_next and not args.only:
+        next_rows = {}
+        views = {"uint8": buf4.view(torch.uint8), "int16": buf4.view(torch.int16),
+                 "float16": buf4.view(torch.float16), "bool": buf4.view(torch.bool), "float32": outs["float32"]}
+        for spec in next_specs():
+            out = views[spec.kind][:n]
+            for _ in range(3):
+                spec.call(rng, out, base, stream)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(max(args.steps, 5))]
+            for a, b in evs:
+                a.record(stream)
+                spec.call(rng, out, base, stream)
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            gbs = spec.written * n / (ms / 1e3) / 1e9
+            next_rows[spec.name] = {"ms": round(ms, 4), "gib_s_written": round(spec.written * n / (ms / 1e3) / GIB, 1),
+                                    "frac_of_hbm": round(gbs / peak, 3), "kernel": spec.kernel}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(rng, torch, specs, outs, (host_x, host_dy), x, dy, n, stream, barrier, dist, dev,
@@ -392,7 +435,8 @@ def run_ours(args):
                        "elements_per_fill": n, "fills_per_step": len(specs), "bytes_written_per_step": written,
                        "l2": "outputs of 1-2 GiB per fill exceed the 129 MB L2; no flush between steps",
                        "parallelism": f"counter-range shards x{world}"},
-            "fills": fills, "roofline": roofline, "slowest_fill": slow, "e2e": e2e, "gpu_launches": launches,
+            "fills": fills, "roofline": roofline, "slowest_fill": slow, "next_rows": next_rows, "e2e": e2e,
+            "gpu_launches": launches,
             "clocks": clocks.summary(),
             "cpu_baseline": None if args.no_cpu else cpu_baseline(specs),
         }
@@ -487,6 +531,7 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=1 << 20, help="oracle elements per fill and step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the fills beyond the step")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("at least 3 warm-up steps")

@@ -36,12 +36,17 @@ _FILL_SIGS = {
     "rng_fill_u64": [_u32, _u32, _sz, _p, _p],
     "rng_fill_f32": [_u32, _u32, _sz, _p, _p],
     "rng_fill_f64": [_u32, _u32, _sz, _p, _p],
+    "rng_fill_u8": [_u32, _u32, _sz, _p, _p],
+    "rng_fill_u16": [_u32, _u32, _sz, _p, _p],
+    "rng_fill_f16": [_u32, _u32, _sz, _p, _p],
+    "rng_fill_bool": [_u32, _u32, _sz, _p, _p],
     "rng_fill_u32_below": [_u32, _u32, _sz, _u32, _p, _p],
     "rng_fill_u64_below": [_u32, _u32, _sz, _u64, _p, _p],
     "rng_fill_i32_range": [_u32, _u32, _sz, _i32, _u32, _p, _p],
     "rng_fill_i64_range32": [_u32, _u32, _sz, _i64, _u32, _p, _p],
     "rng_fill_i64_range": [_u32, _u32, _sz, _i64, _u64, _p, _p],
     "rng_fill_normal_f32": [_u32, _u32, _sz, _p, _p],
+    "rng_fill_normal_f32_pairs": [_u32, _u32, _sz, _p, _p],
     "rng_fill_normal_f64": [_u32, _u32, _sz, _p, _p],
     "rng_fill_normal_f64_noalloc": [_u32, _u32, _sz, _p, _p],
     "rng_dropout_fwd": [_p, _p, _f32, _u32, _u32, _sz, _p],
@@ -85,7 +90,8 @@ def raw(name: str):
 # ---- tensor marshalling -------------------------------------------------------
 _ALLOWED = {
     "u32": ("uint32", "int32"), "u64": ("uint64", "int64"), "i32": ("int32",), "i64": ("int64",),
-    "f32": ("float32",), "f64": ("float64",),
+    "f32": ("float32",), "f64": ("float64",), "u8": ("uint8", "int8", "bool"), "u16": ("uint16", "int16"),
+    "f16": ("float16", "uint16", "int16"),
 }
 
 
@@ -129,6 +135,22 @@ def rng_fill_f64(seed, first_counter, out, stream=None):
     return _fill("rng_fill_f64", "f64", seed, first_counter, out, stream)
 
 
+def rng_fill_u8(seed, first_counter, out, stream=None):
+    return _fill("rng_fill_u8", "u8", seed, first_counter, out, stream)
+
+
+def rng_fill_u16(seed, first_counter, out, stream=None):
+    return _fill("rng_fill_u16", "u16", seed, first_counter, out, stream)
+
+
+def rng_fill_f16(seed, first_counter, out, stream=None):
+    return _fill("rng_fill_f16", "f16", seed, first_counter, out, stream)
+
+
+def rng_fill_bool(seed, first_counter, out, stream=None):
+    return _fill("rng_fill_bool", "u8", seed, first_counter, out, stream)
+
+
 def rng_fill_u32_below(seed, first_counter, bound, out, stream=None):
     return _fill("rng_fill_u32_below", "u32", seed, first_counter, out, stream, bound)
 
@@ -151,6 +173,10 @@ def rng_fill_i64_range(seed, first_counter, low, bound, out, stream=None):
 
 def rng_fill_normal_f32(seed, first_counter, out, stream=None):
     return _fill("rng_fill_normal_f32", "f32", seed, first_counter, out, stream)
+
+
+def rng_fill_normal_f32_pairs(seed, first_counter, out, stream=None):
+    return _fill("rng_fill_normal_f32_pairs", "f32", seed, first_counter, out, stream)
 
 
 def rng_fill_normal_f64(seed, first_counter, out, stream=None):

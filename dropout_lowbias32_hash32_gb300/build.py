@@ -43,7 +43,7 @@ def _flags(verbose: bool) -> list[str]:
 def _compile(src: str, verbose: bool) -> tuple[str, str]:
     obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
     deps = [src] + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
-        glob.glob(os.path.join(CSRC, "*.inc")) + [os.path.join(ROOT, "include", "rng.h")]
+        glob.glob(os.path.join(CSRC, "*.inc")) + glob.glob(os.path.join(ROOT, "include", "*"))
     if not verbose and os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(d) for d in deps):
         return obj, ""
     proc = subprocess.run([nvcc(), *_flags(verbose), "-c", src, "-o", obj], capture_output=True, text=True)

@@ -170,6 +170,38 @@ rng_status rng_fill_f64(uint32_t seed, uint32_t first_counter, size_t n, double 
     });
 }
 
+rng_status rng_fill_u8(uint32_t seed, uint32_t first_counter, size_t n, uint8_t *out, void *stream)
+{
+    const uint32_t key = seed_key(seed);
+    return fill("rng_fill_u8", first_counter, n, out, [&](uint32_t c, uint32_t len, uint8_t *o) {
+        return launch_fill_u8(key, c, len, o, RNG_STREAM(stream));
+    });
+}
+
+rng_status rng_fill_u16(uint32_t seed, uint32_t first_counter, size_t n, uint16_t *out, void *stream)
+{
+    const uint32_t key = seed_key(seed);
+    return fill("rng_fill_u16", first_counter, n, out, [&](uint32_t c, uint32_t len, uint16_t *o) {
+        return launch_fill_u16(key, c, len, o, RNG_STREAM(stream));
+    });
+}
+
+rng_status rng_fill_f16(uint32_t seed, uint32_t first_counter, size_t n, uint16_t *out, void *stream)
+{
+    const uint32_t key = seed_key(seed);
+    return fill("rng_fill_f16", first_counter, n, out, [&](uint32_t c, uint32_t len, uint16_t *o) {
+        return launch_fill_f16(key, c, len, o, RNG_STREAM(stream));
+    });
+}
+
+rng_status rng_fill_bool(uint32_t seed, uint32_t first_counter, size_t n, uint8_t *out, void *stream)
+{
+    const uint32_t key = seed_key(seed);
+    return fill("rng_fill_bool", first_counter, n, out, [&](uint32_t c, uint32_t len, uint8_t *o) {
+        return launch_fill_bool(key, c, len, o, RNG_STREAM(stream));
+    });
+}
+
 rng_status rng_fill_u32_below(uint32_t seed, uint32_t first_counter, size_t n, uint32_t bound, uint32_t *out,
                               void *stream)
 {
@@ -225,6 +257,14 @@ rng_status rng_fill_normal_f32(uint32_t seed, uint32_t first_counter, size_t n, 
     const uint32_t key = seed_key(seed);
     return fill("rng_fill_normal_f32", first_counter, n, out, [&](uint32_t c, uint32_t len, float *o) {
         return launch_fill_normal_f32(key, c, len, o, RNG_STREAM(stream));
+    });
+}
+
+rng_status rng_fill_normal_f32_pairs(uint32_t seed, uint32_t first_counter, size_t n, float *out, void *stream)
+{
+    const uint32_t key = seed_key(seed);
+    return fill("rng_fill_normal_f32_pairs", first_counter, n, out, [&](uint32_t c, uint32_t len, float *o) {
+        return launch_fill_normal_f32_pairs(key, c, len, o, RNG_STREAM(stream));
     });
 }
 

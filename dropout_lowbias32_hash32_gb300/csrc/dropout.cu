@@ -8,9 +8,9 @@
 // uniform(seed, c) >= p  <=>  (D32 & 0x7FFFFF) >= T with T = ceil(p 2^23):
 // the uniform is exactly m 2^-23 and p 2^23 is exact in binary64, so the
 // integer compare (threshold from the host) decides exactly as the f32
-// compare.  The kept value is the IEEE quotient x / (1 - p) (this file is
-// built without fast-math: '/' is the correctly rounded division) with
-// 1 - p rounded to f32 on the host.  Dropped elements are +0.
+// compare.  The kept value is the IEEE quotient x / (1 - p) (__fdiv_rn) with
+// 1 - p rounded to f32 on the host.  Dropped elements are +0.  The element
+// function is lowbias32::dropout of include/rng_device.cuh.
 //
 // When x and y share their offset within 16 bytes, every thread moves one
 // 16-byte vector in and one out (warps read and write 512 contiguous bytes);
@@ -25,8 +25,7 @@ namespace {
 
 __device__ __forceinline__ float drop(float x, uint32_t key, uint32_t threshold, float divisor, uint32_t c)
 {
-    const bool keep = (draw32(key, c) & 0x7FFFFFu) >= threshold;
-    return keep ? x / divisor : 0.0f;
+    return lowbias32::dropout(lowbias32::Dropout{lowbias32::Key{key}, threshold, divisor}, x, c);
 }
 
 __global__ void __launch_bounds__(kFillThreads)

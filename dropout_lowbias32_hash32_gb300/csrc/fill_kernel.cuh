@@ -50,6 +50,33 @@ struct VectorsPerStep<Gen, decltype(void(Gen::kVectorsPerStep))> {
     static constexpr uint32_t value = Gen::kVectorsPerStep;
 };
 
+// A generator may also compute a whole 16-byte vector at once,
+// `Vec16<T> vec(uint32_t c0) const` for the elements at c0 .. c0 + kPer - 1,
+// when neighbouring elements share one draw (the paired normals, the narrow
+// fills); the kernel then calls it for the body and the per-element
+// operator() only for the peeled head and tail.
+template <class Gen, class = void>
+struct HasVec {
+    static constexpr bool value = false;
+};
+template <class Gen>
+struct HasVec<Gen, decltype(void(&Gen::vec))> {
+    static constexpr bool value = true;
+};
+
+template <class Gen>
+__device__ __forceinline__ Vec16<typename Gen::T> gen_vec(const Gen &gen, uint32_t c)
+{
+    if constexpr (HasVec<Gen>::value) {
+        return gen.vec(c);
+    } else {
+        Vec16<typename Gen::T> x;
+#pragma unroll
+        for (uint32_t k = 0; k < Vec16<typename Gen::T>::kPer; ++k) x.v[k] = gen(c + k);
+        return x;
+    }
+}
+
 template <class Gen>
 __global__ void __launch_bounds__(kFillThreads)
 fill_kernel(Gen gen, typename Gen::T *__restrict__ out, uint32_t first, uint32_t head, uint32_t n_vec,
@@ -69,24 +96,13 @@ fill_kernel(Gen gen, typename Gen::T *__restrict__ out, uint32_t first, uint32_t
     uint32_t v = tid;
     if (VectorsPerStep<Gen>::value == 2) {
         for (; v + stride < n_vec; v += 2u * stride) {
-            Vec16<T> x, y;
-            const uint32_t cx = c0 + v * kPer, cy = c0 + (v + stride) * kPer;
-#pragma unroll
-            for (uint32_t k = 0; k < kPer; ++k) {
-                x.v[k] = gen(cx + k);
-                y.v[k] = gen(cy + k);
-            }
+            const Vec16<T> x = gen_vec(gen, c0 + v * kPer);
+            const Vec16<T> y = gen_vec(gen, c0 + (v + stride) * kPer);
             store16(body + v * kPer, x);
             store16(body + (v + stride) * kPer, y);
         }
     }
-    for (; v < n_vec; v += stride) {
-        Vec16<T> x;
-        const uint32_t c = c0 + v * kPer;
-#pragma unroll
-        for (uint32_t k = 0; k < kPer; ++k) x.v[k] = gen(c + k);
-        store16(body + v * kPer, x);
-    }
+    for (; v < n_vec; v += stride) store16(body + v * kPer, gen_vec(gen, c0 + v * kPer));
 }
 
 // Launch one piece of n elements (n <= kChunk).

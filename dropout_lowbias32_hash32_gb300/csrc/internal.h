@@ -52,6 +52,10 @@ cudaError_t launch_fill_u32(uint32_t key, uint32_t first, uint32_t n, uint32_t *
 cudaError_t launch_fill_u64(uint32_t key, uint32_t first, uint32_t n, uint64_t *out, cudaStream_t s);
 cudaError_t launch_fill_f32(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
 cudaError_t launch_fill_f64(uint32_t key, uint32_t first, uint32_t n, double *out, cudaStream_t s);
+cudaError_t launch_fill_u8(uint32_t key, uint32_t first, uint32_t n, uint8_t *out, cudaStream_t s);
+cudaError_t launch_fill_u16(uint32_t key, uint32_t first, uint32_t n, uint16_t *out, cudaStream_t s);
+cudaError_t launch_fill_f16(uint32_t key, uint32_t first, uint32_t n, uint16_t *out, cudaStream_t s);
+cudaError_t launch_fill_bool(uint32_t key, uint32_t first, uint32_t n, uint8_t *out, cudaStream_t s);
 
 struct Below32Args {
     uint32_t key, purpose_key, bound, threshold;
@@ -72,6 +76,7 @@ cudaError_t launch_fill_i64_range(const Below64Args &a, int64_t low, uint32_t fi
                                   int64_t *out, cudaStream_t s);
 
 cudaError_t launch_fill_normal_f32(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
+cudaError_t launch_fill_normal_f32_pairs(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
 
 // Dropout of one piece: keep iff (D32 & 0x7FFFFF) >= threshold, y = x / divisor.
 cudaError_t launch_dropout(const float *x, float *y, uint32_t key, uint32_t threshold, float divisor,

@@ -4,72 +4,66 @@
 // cos(6.283185307179586 u1), u0 = uniform(seed, 2c), u1 = uniform(seed,
 // 2c + 1); one value per counter (the cosine branch).
 //
-// Evaluation in f32, on the instruction budget of an HBM-speed fill:
-//   1 - u0 = 2 - (1 + u0) from the pattern 0x3F800000 | m0, exact, in (0, 1];
-//   L = ln(1 - u0): for u0 < 2^-5 the series -(u + u^2/2 + ... + u^5/5)
-//   (Mercator series; relative error below 1e-7 there, where the radius is
-//   small and an absolutely accurate log is not enough), otherwise
-//   ln 2 * log2(1 - u0) from the hardware log2 (absolute error <= 2^-22 on
-//   [1/2, 1], i.e. radius error <= 7e-7 for radii >= 1/4);
-//   radius = sqrt(t), t = -2L, from the hardware square root (t is 0 or at
-//   least 2^-22, never subnormal, so the flush-to-zero forms lose nothing);
-//   cos(2 pi u1) = -cos(2 pi (u1 - 1/2)) with u1 - 1/2 = (1 + u1) - 3/2 exact,
-//   so the hardware cosine runs on [-pi, pi), where its absolute error is
-//   below 2^-21.4 (tandem-sycl "Design", section Normals: the angle shifted
-//   by half a turn).
-// Every value is within 4e-6 (1 + |z|) of the exact z.
+// Evaluated by lowbias32::randn (include/rng_device.cuh), in f32 on the
+// instruction budget of an HBM-speed fill: 1 - u0 exact; ln(1 - u0) from the
+// Mercator series below u0 = 2^-5 and the hardware log2 above; the hardware
+// sqrt; cos(2 pi u1) = -cos(2 pi (u1 - 1/2)) so the hardware cosine runs on
+// [-pi, pi) (tandem-sycl "Design", section Normals: the angle shifted by half
+// a turn).  Every value is within 4e-6 (1 + |z|) of the exact z.
 #include "fill_kernel.cuh"
 #include "hash32.cuh"
 
 namespace rngk {
 namespace {
 
-// Hardware approximations (PTX .approx, flush-to-zero: no operand here is
-// subnormal).
-__device__ __forceinline__ float lg2_approx(float x)
-{
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float sqrt_approx(float x)
-{
-    float y;
-    asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float cos_approx(float x)
-{
-    float y;
-    asm("cos.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 struct GenNormalF32 {
     using T = float;
     static constexpr uint32_t kVectorsPerStep = 2;
     uint32_t key;  // folded hash of the seed
-    __device__ T operator()(uint32_t c) const
+    __device__ T operator()(uint32_t c) const { return lowbias32::randn(lowbias32::Key{key}, c); }
+};
+
+// Paired normals: element c is the cosine branch of pair c >> 1 (even c)
+// or its sine branch (odd c), pair q Box-Muller on the uniforms at 2q and
+// 2q + 1; one 64-bit draw, one radius and one angle serve two elements.  A
+// vector's four counters start at the same parity everywhere in a launch
+// (c0 = first + head + 4v), so the branch below is uniform across the grid;
+// an odd start needs three pairs per vector instead of two.
+struct GenNormalF32Pairs {
+    using T = float;
+    static constexpr uint32_t kVectorsPerStep = 2;
+    uint32_t key;
+    __device__ T operator()(uint32_t c) const { return lowbias32::randn_paired(lowbias32::Key{key}, c); }
+    __device__ Vec16<float> vec(uint32_t c0) const
     {
-        const Words h = draw64_words(key, c);  // the draws at 2c and 2c + 1
-        const float one_plus_u0 = __uint_as_float(0x3F800000u | (h.hi & 0x7FFFFFu));
-        const float u0 = one_plus_u0 - 1.0f;
-        const float v = 2.0f - one_plus_u0;  // 1 - u0
-        float series = __fmaf_rn(u0, 0.2f, 0.25f);
-        series = __fmaf_rn(u0, series, 0.333333343f);
-        series = __fmaf_rn(u0, series, 0.5f);
-        series = __fmaf_rn(u0, series, 1.0f);
-        const float minus_two_l_small = (2.0f * u0) * series;         // -2 ln(1 - u0), u0 small
-        const float minus_two_l_large = -1.38629436f * lg2_approx(v);  // -2 ln 2 log2(1 - u0)
-        const float t = (h.hi & 0x7C0000u) ? minus_two_l_large : minus_two_l_small;  // u0 >= 2^-5 ?
-        const float u1_minus_half = __uint_as_float(0x3F800000u | (h.lo & 0x7FFFFFu)) - 1.5f;
-        return -sqrt_approx(t) * cos_approx(u1_minus_half * 6.28318530717958647692f);
+        const lowbias32::Key k{key};
+        Vec16<float> x;
+        if ((c0 & 1u) == 0u) {
+            const float2 a = lowbias32::randn_pair(k, c0 >> 1);
+            const float2 b = lowbias32::randn_pair(k, (c0 + 2u) >> 1);
+            x.v[0] = a.x;
+            x.v[1] = a.y;
+            x.v[2] = b.x;
+            x.v[3] = b.y;
+        } else {
+            const float2 a = lowbias32::randn_pair(k, c0 >> 1);
+            const float2 b = lowbias32::randn_pair(k, (c0 + 1u) >> 1);
+            const float2 d = lowbias32::randn_pair(k, (c0 + 3u) >> 1);
+            x.v[0] = a.y;
+            x.v[1] = b.x;
+            x.v[2] = b.y;
+            x.v[3] = d.x;
+        }
+        return x;
     }
 };
 
 }  // namespace
+
+cudaError_t launch_fill_normal_f32_pairs(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s)
+{
+    return launch_fill(GenNormalF32Pairs{key}, out, first, n, s);
+}
 
 cudaError_t launch_fill_normal_f32(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s)
 {

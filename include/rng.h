@@ -75,6 +75,25 @@ rng_status rng_fill_f32(uint32_t seed, uint32_t first_counter, size_t n, float *
 rng_status rng_fill_f64(uint32_t seed, uint32_t first_counter, size_t n, double *out,
                         void *stream);
 
+/* ---- narrow fills ----------------------------------------------------------- */
+/* (tandem-cuda "Performance", rows fill_u16, fill_f16_bits, fill_u8 and
+ * fill_bool, restated on hash32.)  Each element stays a pure function of its
+ * counter; one 32-bit draw serves 4, 2 or 32 consecutive counters, the word
+ * index wrapping with the counter. */
+
+/* out[i] = byte (c_i & 3) of D32(seed, c_i >> 2), bits 8(c_i & 3) .. +7. */
+rng_status rng_fill_u8(uint32_t seed, uint32_t first_counter, size_t n, uint8_t *out, void *stream);
+
+/* out[i] = halfword (c_i & 1) of D32(seed, c_i >> 1), bits 16(c_i & 1) .. +15. */
+rng_status rng_fill_u16(uint32_t seed, uint32_t first_counter, size_t n, uint16_t *out, void *stream);
+
+/* out[i] = binary16 bits of m 2^-10, m the low 10 bits of the u16 element at
+ * c_i: a uniform on the 2^-10 grid in [0, 1), exactly. */
+rng_status rng_fill_f16(uint32_t seed, uint32_t first_counter, size_t n, uint16_t *out, void *stream);
+
+/* out[i] = bit (c_i & 31) of D32(seed, c_i >> 5), one byte (0 or 1) per bit. */
+rng_status rng_fill_bool(uint32_t seed, uint32_t first_counter, size_t n, uint8_t *out, void *stream);
+
 /* ---- bounded integers: Lemire's multiply-shift with rejection ------------ */
 /* (perturbation-kernel "Backends", section "Why the GPU can be exact";
  * tandem-cuda "Performance", bounded rows.)  For a w-bit word x the candidate
@@ -119,6 +138,17 @@ rng_status rng_fill_i64_range(uint32_t seed, uint32_t first_counter, size_t n, i
  * value is within 4e-6 (1 + |z|) of the exact z. */
 rng_status rng_fill_normal_f32(uint32_t seed, uint32_t first_counter, size_t n, float *out,
                                void *stream);
+
+/* Paired Box-Muller: both branches of each uniform pair, one 64-bit draw
+ * per two values (half the hashing of rng_fill_normal_f32).  With q = c_i >> 1,
+ * u0 = uniform(seed, 2q), u1 = uniform(seed, 2q + 1), r = sqrt(-2 ln(1 - u0)):
+ * out[i] = r cos(2 pi u1) for even c_i (= randn(seed, q)), r sin(2 pi u1) for
+ * odd c_i.  The pages' randn keeps the cosine branch only (Phobos "Random
+ * numbers", section randn); tandem-sycl "Design", section Normals, draws
+ * Box-Muller pairs.  Same accuracy as rng_fill_normal_f32: within
+ * 4e-6 (1 + |z|) of the exact value. */
+rng_status rng_fill_normal_f32_pairs(uint32_t seed, uint32_t first_counter, size_t n, float *out,
+                                     void *stream);
 
 /* out[i] = standard normal from the 1024-layer Marsaglia-Tsang ziggurat on
  * the 64-bit draw D64(seed, c_i) (tandem-sycl "Design", section Normals).

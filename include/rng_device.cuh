@@ -1,0 +1,203 @@
+// rng_device.cuh -- device-side lowbias32 draws, for fusing random numbers
+// into user kernels (a dropout in a GEMM epilogue, noise in an attention
+// kernel) with no stored mask and no extra pass over memory.
+//
+// Every value is a pure function of (seed, counter), the same function the
+// C ABI's fills compute (include/rng.h):
+//   hash32 = lowbias32 (Phobos stdlib "Random numbers", section hash32);
+//   draw32(k, c) = hash32(c ^ hash32(seed))             (section uniform);
+//   uniform      = (draw32 & 0x7FFFFF) * 2^-23         (section uniform);
+//   randn        = sqrt(-2 ln(1 - u(2c))) cos(2 pi u(2c + 1))  (section randn);
+//   dropout      = uniform >= p ? x / (1 - p) : 0       (section dropout).
+// A kernel that gives element e the counter first + e draws exactly what
+// the corresponding fill writes: dropout() is bit-identical to
+// rng_dropout_fwd, uniform() to rng_fill_f32, draw32() to rng_fill_u32;
+// randn() is the value rng_fill_normal_f32 writes.  The page's advice holds:
+// use each element's flat index as its counter, and give different uses of
+// one seed disjoint counters (randn reads the uniforms at 2c and 2c + 1).
+//
+// Keys are made once on the host (make_key, make_dropout) and passed to the
+// kernel by value.  The header needs only <stdint.h> and nvcc.
+#pragma once
+
+#include <stdint.h>
+
+namespace lowbias32 {
+
+// ---- the hash -----------------------------------------------------------
+
+// hash32 after its first xorshift: two multiply-xorshift rounds.
+__host__ __device__ __forceinline__ uint32_t hash32_rounds(uint32_t x)
+{
+    x *= 0x7FEB352Du;  // 2146121005
+    x ^= x >> 15;
+    x *= 0x846CA68Bu;  // -2073254261 as a bit pattern
+    x ^= x >> 16;
+    return x;
+}
+
+// lowbias32: logical xorshifts by 16, 15, 16 around two wrapping multiplies.
+__host__ __device__ __forceinline__ uint32_t hash32(uint32_t x) { return hash32_rounds(x ^ (x >> 16)); }
+
+// A seed's key: hash32(seed) folded into hash32's first xorshift,
+// (c ^ k) ^ ((c ^ k) >> 16) = c ^ (c >> 16) ^ (k ^ (k >> 16)).
+struct Key {
+    uint32_t folded;
+};
+
+__host__ __device__ __forceinline__ Key key_of_hash(uint32_t k) { return Key{k ^ (k >> 16)}; }
+__host__ __device__ __forceinline__ Key make_key(uint32_t seed) { return key_of_hash(hash32(seed)); }
+
+// ---- draws ----------------------------------------------------------------
+
+// hash32(c ^ hash32(seed))
+__host__ __device__ __forceinline__ uint32_t draw32(Key k, uint32_t c)
+{
+    return hash32_rounds(c ^ (c >> 16) ^ k.folded);
+}
+
+// The two words of the 64-bit draw at c: the draws at 2c (hi) and 2c + 1
+// (lo), counters mod 2^32.  2c + 1 = 2c ^ 1 and bit 0 never reaches the
+// shifted term, so the low word's first xorshift is the high word's ^ 1.
+struct Words {
+    uint32_t hi, lo;
+};
+
+__host__ __device__ __forceinline__ Words draw64_words(Key k, uint32_t c)
+{
+    const uint32_t a = c << 1;
+    const uint32_t first = a ^ (a >> 16) ^ k.folded;
+    return Words{hash32_rounds(first), hash32_rounds(first ^ 1u)};
+}
+
+__host__ __device__ __forceinline__ uint64_t draw64(Key k, uint32_t c)
+{
+    const Words w = draw64_words(k, c);
+    return (static_cast<uint64_t>(w.hi) << 32) | w.lo;
+}
+
+// ---- uniforms ---------------------------------------------------------------
+
+// (draw32 & 0x7FFFFF) * 2^-23, exactly: 0x3F800000 | m is 1 + m 2^-23 and
+// subtracting 1 is exact.
+__device__ __forceinline__ float uniform_of(uint32_t d)
+{
+    return __uint_as_float(0x3F800000u | (d & 0x7FFFFFu)) - 1.0f;
+}
+
+__device__ __forceinline__ float uniform(Key k, uint32_t c) { return uniform_of(draw32(k, c)); }
+
+// ---- randn (Box-Muller, cosine branch) --------------------------------------
+
+namespace detail {
+__device__ __forceinline__ float lg2_approx(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float sqrt_approx(float x)
+{
+    float y;
+    asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float cos_approx(float x)
+{
+    float y;
+    asm("cos.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float sin_approx(float x)
+{
+    float y;
+    asm("sin.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The Box-Muller radius sqrt(-2 ln(1 - u0)) from the draw d0 at 2c.
+// 1 - u0 = 2 - (1 + u0), exact, in (0, 1].  For u0 < 2^-5 the Mercator
+// series -(u + u^2/2 + ... + u^5/5) (relative error < 1e-7 where the radius
+// is small and an absolutely accurate log is not enough); above, ln 2 times
+// the hardware log2 (absolute error <= 2^-22 on [1/2, 1]).
+__device__ __forceinline__ float box_muller_radius(uint32_t d0)
+{
+    const float one_plus_u0 = __uint_as_float(0x3F800000u | (d0 & 0x7FFFFFu));
+    const float u0 = one_plus_u0 - 1.0f;
+    const float v = 2.0f - one_plus_u0;
+    float series = __fmaf_rn(u0, 0.2f, 0.25f);
+    series = __fmaf_rn(u0, series, 0.333333343f);
+    series = __fmaf_rn(u0, series, 0.5f);
+    series = __fmaf_rn(u0, series, 1.0f);
+    const float small = (2.0f * u0) * series;      // -2 ln(1 - u0), u0 < 2^-5
+    const float large = -1.38629436f * lg2_approx(v);  // -2 ln 2 log2(1 - u0)
+    return sqrt_approx((d0 & 0x7C0000u) ? large : small);
+}
+
+// The angle 2 pi (u1 - 1/2) in [-pi, pi) from the draw d1 at 2c + 1, with
+// u1 - 1/2 = (1 + u1) - 3/2 exact: cos(2 pi u1) = -cos(angle),
+// sin(2 pi u1) = -sin(angle).
+__device__ __forceinline__ float box_muller_angle(uint32_t d1)
+{
+    return (__uint_as_float(0x3F800000u | (d1 & 0x7FFFFFu)) - 1.5f) * 6.28318530717958647692f;
+}
+}  // namespace detail
+
+// randn(seed, c) in f32, within 4e-6 (1 + |z|) of the exact value.
+__device__ __forceinline__ float randn(Key k, uint32_t c)
+{
+    const Words w = draw64_words(k, c);  // the draws at 2c and 2c + 1
+    return -detail::box_muller_radius(w.hi) * detail::cos_approx(detail::box_muller_angle(w.lo));
+}
+
+// Both Box-Muller branches of pair q (the uniforms at 2q and 2q + 1):
+// x = r cos(2 pi u1), y = r sin(2 pi u1); x equals randn(k, q).  One
+// 64-bit draw per two values.
+__device__ __forceinline__ float2 randn_pair(Key k, uint32_t q)
+{
+    const Words w = draw64_words(k, q);
+    const float r = detail::box_muller_radius(w.hi);
+    const float a = detail::box_muller_angle(w.lo);
+    return make_float2(-r * detail::cos_approx(a), -r * detail::sin_approx(a));
+}
+
+// The element with counter c of the paired normal fill: the cosine branch of
+// pair c >> 1 for even c, its sine branch for odd c.
+__device__ __forceinline__ float randn_paired(Key k, uint32_t c)
+{
+    const float2 v = randn_pair(k, c >> 1);
+    return (c & 1u) ? v.y : v.x;
+}
+
+// ---- dropout ------------------------------------------------------------------
+
+// Parameters of one dropout (seed, p): keep iff (draw32 & 0x7FFFFF) >=
+// threshold = ceil(p 2^23) (uniform >= p, exactly), kept values x / divisor
+// with divisor = 1 - p rounded to f32.
+struct Dropout {
+    Key key;
+    uint32_t threshold;
+    float divisor;
+};
+
+// Host side: p must lie in [0, 1).
+inline Dropout make_dropout(uint32_t seed, float p)
+{
+    const double scaled = static_cast<double>(p) * 8388608.0;  // exact
+    uint32_t t = static_cast<uint32_t>(scaled);
+    if (static_cast<double>(t) < scaled) ++t;  // ceil
+    return Dropout{make_key(seed), t, 1.0f - p};
+}
+
+__device__ __forceinline__ bool dropout_keep(const Dropout &d, uint32_t c)
+{
+    return (draw32(d.key, c) & 0x7FFFFFu) >= d.threshold;
+}
+
+// The element with counter c of dropout(x, p, seed, c): IEEE x / (1 - p) or +0.
+__device__ __forceinline__ float dropout(const Dropout &d, float x, uint32_t c)
+{
+    return dropout_keep(d, c) ? __fdiv_rn(x, d.divisor) : 0.0f;
+}
+
+}  // namespace lowbias32

@@ -63,12 +63,18 @@ _SIGS = {
     "orc_fill_u64": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_fill_f32": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_fill_f64": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_u8": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_u16": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_bool": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_f16_bits": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_fill_u32_below": (None, [_u32, _u32, _sz, _p, _u32, _p]),
     "orc_fill_u64_below": (None, [_u32, _u32, _sz, _p, _u64, _p]),
     "orc_fill_i32_range": (None, [_u32, _u32, _sz, _p, _i32, _u32, _p]),
     "orc_fill_i64_range32": (None, [_u32, _u32, _sz, _p, _i64, _u32, _p]),
     "orc_fill_i64_range": (None, [_u32, _u32, _sz, _p, _i64, _u64, _p]),
     "orc_fill_randn": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_randn_paired": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_randn_paired": (_f64, [_u32, _u32]),
     "orc_fill_normal_f64": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_dropout_fill": (None, [_p, _f32, _u32, _u32, _sz, _p, _p]),
     "orc_fill_zig_fast": (None, [_u32, _u32, _sz, _p, _p]),
@@ -191,6 +197,18 @@ class Oracle:
     def fill_f64(self, seed, first, n=None, idx=None):
         return self._fill("orc_fill_f64", np.float64, seed, first, n, idx)
 
+    def fill_u8(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_u8", np.uint8, seed, first, n, idx)
+
+    def fill_u16(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_u16", np.uint16, seed, first, n, idx)
+
+    def fill_bool(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_bool", np.uint8, seed, first, n, idx)
+
+    def fill_f16_bits(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_f16_bits", np.uint16, seed, first, n, idx)
+
     def fill_u32_below(self, seed, first, bound, n=None, idx=None):
         return self._fill("orc_fill_u32_below", np.uint32, seed, first, n, idx, bound)
 
@@ -209,6 +227,10 @@ class Oracle:
     def fill_randn(self, seed, first, n=None, idx=None):
         """binary64 values of the randn definition (not rounded to f32)."""
         return self._fill("orc_fill_randn", np.float64, seed, first, n, idx)
+
+    def fill_randn_paired(self, seed, first, n=None, idx=None):
+        """binary64 values of the paired Box-Muller definition."""
+        return self._fill("orc_fill_randn_paired", np.float64, seed, first, n, idx)
 
     def fill_normal_f64(self, seed, first, n=None, idx=None):
         return self._fill("orc_fill_normal_f64", np.float64, seed, first, n, idx)

@@ -100,6 +100,38 @@ double orc_uniform_f64(uint32_t seed, uint32_t counter)
     return (double)(orc_draw64(seed, counter) >> 11) * 0x1p-53;
 }
 
+/* Narrow draws [Tandem-P, rows fill_u16, fill_f16_bits, fill_u8, fill_bool]:
+ * element c is a byte, halfword or bit of the 32-bit draw at c >> 2, c >> 1
+ * or c >> 5, least significant first.  READING: this layout. */
+uint8_t orc_u8(uint32_t seed, uint32_t counter)
+{
+    return (uint8_t)(orc_draw32(seed, counter >> 2) >> (8u * (counter & 3u)));
+}
+
+uint16_t orc_u16(uint32_t seed, uint32_t counter)
+{
+    return (uint16_t)(orc_draw32(seed, counter >> 1) >> (16u * (counter & 1u)));
+}
+
+uint8_t orc_bool(uint32_t seed, uint32_t counter)
+{
+    return (uint8_t)((orc_draw32(seed, counter >> 5) >> (counter & 31u)) & 1u);
+}
+
+/* binary16 bits of m 2^-10, m the low 10 bits of the u16 element: zero, or
+ * 2^(p-10) (1 + f) with p the position of m's leading one, biased exponent
+ * p - 10 + 15, and the 10 bits of m below its leading one as the fraction.
+ * READING: the f16 fill as a uniform on the 2^-10 grid. */
+uint16_t orc_f16_bits(uint32_t seed, uint32_t counter)
+{
+    uint32_t m = orc_u16(seed, counter) & 0x3FFu;
+    if (m == 0) return 0;
+    unsigned p = 0;
+    while ((m >> (p + 1)) != 0) ++p;
+    uint32_t fraction = (m << (10u - p)) & 0x3FFu;
+    return (uint16_t)(((p + 5u) << 10) | fraction);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Substreams for retries and ziggurat misses [Tandem-D, section Normals:     */
 /* a draw that misses continues on split(g) of sub(PURPOSE) of the key, g the */
@@ -196,6 +228,20 @@ double orc_randn(uint32_t seed, uint32_t counter)
     double u0 = (double)orc_uniform_f32(seed, 2u * counter);
     double u1 = (double)orc_uniform_f32(seed, 2u * counter + 1u);
     return sqrt(-2.0 * log(1.0 - u0)) * cos(6.283185307179586 * u1);
+}
+
+/* Paired Box-Muller (both branches of one uniform pair, as the tandem
+ * pages draw pairs [Tandem-D, section Normals]): element c takes pair
+ * q = c >> 1, the uniforms at 2q and 2q + 1, and the cosine branch for even
+ * c (randn at counter q) or the sine branch for odd c.  READING: this
+ * counter layout. */
+double orc_randn_paired(uint32_t seed, uint32_t counter)
+{
+    uint32_t q = counter >> 1;
+    double u0 = (double)orc_uniform_f32(seed, 2u * q);
+    double u1 = (double)orc_uniform_f32(seed, 2u * q + 1u);
+    double r = sqrt(-2.0 * log(1.0 - u0));
+    return (counter & 1u) ? r * sin(6.283185307179586 * u1) : r * cos(6.283185307179586 * u1);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -473,6 +519,26 @@ void orc_fill_f64(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, 
     for (size_t i = 0; i < n; ++i) out[i] = orc_uniform_f64(seed, counter_of(first, idx, i));
 }
 
+void orc_fill_u8(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint8_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_u8(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_u16(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint16_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_u16(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_bool(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint8_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_bool(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_f16_bits(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint16_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_f16_bits(seed, counter_of(first, idx, i));
+}
+
 void orc_fill_u32_below(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, uint32_t b,
                         uint32_t *out)
 {
@@ -506,6 +572,11 @@ void orc_fill_i64_range(uint32_t seed, uint32_t first, size_t n, const uint64_t 
 void orc_fill_randn(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)
 {
     for (size_t i = 0; i < n; ++i) out[i] = orc_randn(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_randn_paired(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_randn_paired(seed, counter_of(first, idx, i));
 }
 
 void orc_fill_normal_f64(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)

@@ -87,6 +87,28 @@ def pin_draw64_words(orc):
     assert np.all((f >= 0) & (f < 1))
 
 
+def pin_narrow_fills(orc):
+    """The narrow fills carve the pinned 32-bit draws: four u8 (two u16)
+    elements at counters 4w .. 4w + 3 (2w, 2w + 1) are draw32(seed, w) in
+    little-endian order, and 32 bool elements at 32w .. 32w + 31 are its
+    bits, least significant first; the f16 element is numpy's binary16 of
+    (u16 & 0x3FF) 2^-10, a multiple of 2^-10 in [0, 1); bools are fair."""
+    seed, words = 0x9E3779B9, 4096
+    w = orc.fill_u32(seed, 0, words)
+    assert np.array_equal(orc.fill_u8(seed, 0, 4 * words).view("<u4"), w)
+    assert np.array_equal(orc.fill_u16(seed, 0, 2 * words).view("<u4"), w)
+    bits = orc.fill_bool(seed, 0, 32 * words).reshape(words, 32).astype(np.uint64)
+    assert np.array_equal((bits << np.arange(32, dtype=np.uint64)).sum(axis=1).astype(np.uint32), w)
+    u16 = orc.fill_u16(seed, 5, 1 << 16)
+    f16 = orc.fill_f16_bits(seed, 5, 1 << 16)
+    expect = ((u16 & 0x3FF).astype(np.float64) * 2.0 ** -10).astype(np.float16)
+    assert np.array_equal(f16, expect.view(np.uint16))
+    vals = f16.view(np.float16).astype(np.float64)
+    assert vals.min() >= 0 and vals.max() < 1 and np.all(vals * 1024 == np.floor(vals * 1024))
+    b = orc.fill_bool(seed, 3, 1 << 20)
+    assert abs(b.mean() - 0.5) < 5 * 0.5 / math.sqrt(b.size)
+
+
 # ------------------------------------------------------- bounded integers --
 def pin_lemire_exhaustive_8bit(orc):
     """Over every 8-bit word and every bound 1..255, the multiply-shift with
@@ -245,6 +267,33 @@ def pin_randn_distribution(orc):
     _normal_stats(orc.fill_randn(3, 0, 1 << 22))
 
 
+def pin_randn_paired(orc):
+    """Paired Box-Muller: the even element of pair q is randn(seed, q); both
+    elements share one radius, x^2 + y^2 = -2 ln(1 - u0) (cos^2 + sin^2 = 1),
+    and their angle is 2 pi u1: atan2(y, x) = 2 pi u1 (mod 2 pi); at u1 = 1/4
+    the odd element is +r and the even one 0.  Moments, a 200-bin chi-square
+    and no correlation between the two branches."""
+    n = 1 << 20
+    z = orc.fill_randn_paired(5, 0, 2 * n)
+    x, y = z[0::2], z[1::2]
+    assert np.array_equal(x, orc.fill_randn(5, 0, n))
+    u0 = orc.fill_f32(5, 0, idx=2 * np.arange(n)).astype(np.float64)
+    u1 = orc.fill_f32(5, 0, idx=2 * np.arange(n) + 1).astype(np.float64)
+    assert np.allclose(x * x + y * y, -2.0 * np.log1p(-u0), rtol=1e-12, atol=1e-15)
+    r = np.hypot(x, y)
+    big = r > 1e-3
+    ang = np.mod(np.arctan2(y[big], x[big]), 2 * np.pi)
+    diff = np.abs(ang - 2 * np.pi * u1[big])
+    assert np.all(np.minimum(diff, 2 * np.pi - diff) < 1e-9)
+    quarter = _counters_with_low23(orc, 5, 1, (1 << 21,))[1 << 21]
+    assert quarter.size
+    zq = orc.fill_randn_paired(5, 0, idx=2 * quarter + 1)
+    rq = np.sqrt(-2.0 * np.log1p(-orc.fill_f32(5, 0, idx=2 * quarter).astype(np.float64)))
+    assert np.allclose(zq, rq, rtol=1e-14, atol=0)
+    _normal_stats(y)
+    assert abs(np.corrcoef(x, y)[0, 1]) < 5 / math.sqrt(n)
+
+
 # ---------------------------------------------------------------- dropout --
 def pin_dropout(orc):
     """Phobos 'Random numbers', dropout: where(uniform >= p, x / (1 - p), 0)
@@ -398,6 +447,11 @@ def pin_slice_invariant(orc):
     rng = np.random.default_rng(2)
     n = 3000
     fills = [
+        lambda f, m, idx=None: orc.fill_u8(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_u16(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_bool(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_f16_bits(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_randn_paired(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_u32(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_u64(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_f32(9, f, m, idx),
@@ -422,10 +476,10 @@ def pin_slice_invariant(orc):
 
 
 ALL_PINS = [
-    pin_tile_mean, pin_uniform_grid, pin_hash_bijective, pin_draw64_words,
+    pin_tile_mean, pin_uniform_grid, pin_hash_bijective, pin_draw64_words, pin_narrow_fills,
     pin_lemire_exhaustive_8bit, pin_lemire_exhaustive_16bit, pin_lemire_wide_words,
     pin_below_distributions, pin_ranges_wrap, pin_randn_special_angles,
-    pin_randn_tail_end, pin_randn_distribution, pin_dropout, pin_zexp_zlog,
+    pin_randn_tail_end, pin_randn_distribution, pin_randn_paired, pin_dropout, pin_zexp_zlog,
     pin_zig_table_published, pin_zig_table_invariants, pin_zig_miss_rate,
     pin_normal_f64_distribution, pin_zig_wedge_acceptance, pin_slice_invariant,
 ]

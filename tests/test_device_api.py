@@ -1,0 +1,90 @@
+"""The public device header (include/rng_device.cuh) used the way a fused
+user kernel would use it: kernels compiled against the header alone must
+draw what the oracle defines and what the library's fills write, and the
+Phobos page's dropout_rows tile kernel must equal rng_dropout_fwd."""
+import ctypes as C
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+from helpers import ROOT
+
+SRC = os.path.join(ROOT, "tests", "device_api", "device_api_kernels.cu")
+BUILD = os.path.join(ROOT, "tests", "device_api", "_build")
+U32 = 1 << 32
+
+
+def _nvcc():
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    return None
+
+
+@pytest.fixture(scope="module")
+def devlib():
+    nvcc = _nvcc()
+    if nvcc is None:
+        pytest.skip("nvcc not available")
+    os.makedirs(BUILD, exist_ok=True)
+    so = os.path.join(BUILD, "libdevice_api_kernels.so")
+    if not os.path.exists(so) or os.path.getmtime(so) < max(
+            os.path.getmtime(SRC), os.path.getmtime(os.path.join(ROOT, "include", "rng_device.cuh"))):
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                        "-I" + os.path.join(ROOT, "include"), "-Xcompiler", "-fPIC", "-shared", SRC,
+                        "-o", so + ".tmp"], check=True)
+        os.replace(so + ".tmp", so)
+    lib = C.CDLL(so)
+    lib.device_api_draws.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32] + [C.c_void_p] * 4
+    lib.device_api_dropout_rows.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32, C.c_uint32, C.c_float]
+    lib.device_api_host_hash32.argtypes = [C.c_uint32]
+    lib.device_api_host_hash32.restype = C.c_uint32
+    return lib
+
+
+def test_header_hash_on_the_host_matches_the_oracle(devlib, orc):
+    for x in (0, 1, 2, 0x9E3779B9, U32 - 1, 123456789):
+        assert devlib.device_api_host_hash32(x) == orc.hash32(x)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("first", [0, 3, U32 - 5])
+def test_header_draws_match_the_oracle_and_the_fills(devlib, orc, first):
+    import torch
+
+    import dropout_lowbias32_hash32_gb300 as rng
+    n, seed = 100003, 0x9E3779B9
+    d32 = torch.empty(n, dtype=torch.int32, device="cuda")
+    d64 = torch.empty(n, dtype=torch.int64, device="cuda")
+    u = torch.empty(n, dtype=torch.float32, device="cuda")
+    z = torch.empty(n, dtype=torch.float32, device="cuda")
+    assert devlib.device_api_draws(seed, first, n, d32.data_ptr(), d64.data_ptr(), u.data_ptr(), z.data_ptr()) == 0
+    assert np.array_equal(d32.cpu().numpy().view(np.uint32), orc.fill_u32(seed, first, n))
+    assert np.array_equal(d64.cpu().numpy().view(np.uint64), orc.fill_u64(seed, first, n))
+    assert np.array_equal(u.cpu().numpy().view(np.uint32), orc.fill_f32(seed, first, n).view(np.uint32))
+    ref = orc.fill_randn(seed, first, n)
+    zz = z.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(zz - ref) / (1 + np.abs(ref))) <= 4e-6
+    # the fused draw is the library fill's element, bit for bit
+    lib_z = rng.rng_fill_normal_f32(seed, first, torch.empty(n, dtype=torch.float32, device="cuda"))
+    assert torch.equal(lib_z.view(torch.int32), z.view(torch.int32))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("p", [0.1, 0.5])
+def test_dropout_rows_tile_kernel_equals_the_fused_fill(devlib, orc, p):
+    import torch
+
+    import dropout_lowbias32_hash32_gb300 as rng
+    from dropout_lowbias32_hash32_gb300 import workloads
+    rows = 1003  # a ragged last tile of 16 rows
+    x = workloads.dropout_x(rows * 256)
+    xg = torch.from_numpy(x).cuda()
+    y = torch.empty_like(xg)
+    assert devlib.device_api_dropout_rows(xg.data_ptr(), y.data_ptr(), rows, 42, p) == 0
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), orc.dropout(x, p, 42, 0).view(np.uint32))
+    y_lib = rng.rng_dropout_fwd(xg, torch.empty_like(xg), p, 42, 0)
+    assert torch.equal(y.view(torch.int32), y_lib.view(torch.int32))

@@ -94,12 +94,20 @@ def fills(rng, torch, orc):
                       lambda f, n: orc.fill_i64_range(4, f, -500, 1000, n)),
         "normal_f64": (lambda o, f: rng.rng_fill_normal_f64(7, f, o), t.float64,
                        lambda f, n: orc.fill_normal_f64(7, f, n)),
+        "u8": (lambda o, f: rng.rng_fill_u8(0x9E3779B9, f, o), t.uint8,
+               lambda f, n: orc.fill_u8(0x9E3779B9, f, n)),
+        "u16": (lambda o, f: rng.rng_fill_u16(0x9E3779B9, f, o), t.int16,
+                lambda f, n: orc.fill_u16(0x9E3779B9, f, n).view(np.int16)),
+        "f16": (lambda o, f: rng.rng_fill_f16(0x9E3779B9, f, o), t.int16,
+                lambda f, n: orc.fill_f16_bits(0x9E3779B9, f, n).view(np.int16)),
+        "bool": (lambda o, f: rng.rng_fill_bool(0x9E3779B9, f, o), t.uint8,
+                 lambda f, n: orc.fill_bool(0x9E3779B9, f, n)),
     }
 
 
 FILL_NAMES = ["u32", "u64", "f32", "f64", "u32_below_1000", "u32_below_2^32-2", "u32_below_2^31+1",
               "u64_below_1000", "u64_below_2^64-2", "u64_below_2^63+1", "i32_range", "i32_range_wrap",
-              "i64_range32", "i64_range", "normal_f64"]
+              "i64_range32", "i64_range", "normal_f64", "u8", "u16", "f16", "bool"]
 
 
 @pytest.mark.parametrize("name", FILL_NAMES)
@@ -161,6 +169,27 @@ def test_normal_f32_extreme_radius(rng, torch, orc):
             z = float(_host(rng.rng_fill_normal_f32(7, int(c), out))[0])
             ref = orc.randn(7, int(c))
             assert abs(z - ref) <= 4e-6 * (1 + abs(ref))
+
+
+def test_normal_f32_pairs_within_tolerance(rng, torch, orc):
+    """Paired Box-Muller at every start parity, across the counter wrap and
+    with every output offset: within 4e-6 (1 + |z|) of the oracle, and its
+    even elements equal to rng_fill_normal_f32's values at counter c / 2."""
+    for first in (0, 1, 2, 3, U32 - 5, U32 - 2, U32 - 1):
+        for offset in (0, 1, 2, 3):
+            for n in (1, 2, 3, 5, 17, 4099, 65537):
+                z = _host(rng.rng_fill_normal_f32_pairs(7, first, _out(torch, torch.float32, n, offset)))
+                ref = orc.fill_randn_paired(7, first, n)
+                err = np.abs(z.astype(np.float64) - ref) / (1 + np.abs(ref))
+                assert err.max() <= 4e-6, (first, offset, n, err.max())
+    n = BIG
+    for first in (0, 1):
+        z = _host(rng.rng_fill_normal_f32_pairs(7, first, _out(torch, torch.float32, n, 0)))
+        ref = orc.fill_randn_paired(7, first, n)
+        assert np.max(np.abs(z.astype(np.float64) - ref) / (1 + np.abs(ref))) <= 4e-6
+    pairs = _host(rng.rng_fill_normal_f32_pairs(9, 0, _out(torch, torch.float32, 20000, 0)))
+    cos_branch = _host(rng.rng_fill_normal_f32(9, 0, _out(torch, torch.float32, 10000, 0)))
+    assert np.array_equal(pairs[0::2].view(np.uint32), cos_branch.view(np.uint32))
 
 
 @pytest.mark.parametrize("p", [0.1, 0.5, 0.0, 0.999, 2.0 ** -30])

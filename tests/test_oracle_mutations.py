@@ -16,6 +16,12 @@ MUTATIONS = [
      pins.pin_tile_mean),
     ("24-bit uniform mask", "& 8388607u) * 1.1920928955078125e-7f",
      "& 16777215u) * 1.1920928955078125e-7f", pins.pin_tile_mean),
+    ("u8 byte order", "return (uint8_t)(orc_draw32(seed, counter >> 2) >> (8u * (counter & 3u)));",
+     "return (uint8_t)(orc_draw32(seed, counter >> 2) >> (8u * (3u - (counter & 3u))));", pins.pin_narrow_fills),
+    ("bool bit index", "return (uint8_t)((orc_draw32(seed, counter >> 5) >> (counter & 31u)) & 1u);",
+     "return (uint8_t)((orc_draw32(seed, counter >> 5) >> (31u - (counter & 31u))) & 1u);", pins.pin_narrow_fills),
+    ("f16 exponent", "return (uint16_t)(((p + 5u) << 10) | fraction);", "return (uint16_t)(((p + 6u) << 10) | fraction);",
+     pins.pin_narrow_fills),
     ("64-bit word order",
      "return ((uint64_t)orc_draw32(seed, c2) << 32) | (uint64_t)orc_draw32(seed, c2 + 1u);",
      "return ((uint64_t)orc_draw32(seed, c2 + 1u) << 32) | (uint64_t)orc_draw32(seed, c2);",
@@ -40,6 +46,10 @@ MUTATIONS = [
      pins.pin_randn_special_angles),
     ("randn log(u)", "sqrt(-2.0 * log(1.0 - u0))", "sqrt(-2.0 * log(u0 + 0x1p-24))",
      pins.pin_randn_special_angles),
+    ("paired sine for cosine", "return (counter & 1u) ? r * sin(6.283185307179586 * u1) : r * cos(6.283185307179586 * u1);",
+     "return (counter & 1u) ? r * cos(6.283185307179586 * u1) : r * sin(6.283185307179586 * u1);",
+     pins.pin_randn_paired),
+    ("paired pair index", "    uint32_t q = counter >> 1;", "    uint32_t q = (counter + 1u) >> 1;", pins.pin_randn_paired),
     ("dropout drops ties", "return (u >= p) ? x / keep_scale_divisor : 0.0f;",
      "return (u > p) ? x / keep_scale_divisor : 0.0f;", pins.pin_dropout),
     ("dropout reciprocal multiply", "return (u >= p) ? x / keep_scale_divisor : 0.0f;",
