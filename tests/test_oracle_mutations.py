@@ -36,16 +36,16 @@ MUTATIONS = [
      pins.pin_lemire_exhaustive_8bit),
     ("range without low", "return (int32_t)((uint32_t)low + orc_below32(seed, counter, b));",
      "return (int32_t)orc_below32(seed, counter, b);", pins.pin_ranges_wrap),
-    ("randn sin branch", "* cos(6.283185307179586 * u1);", "* sin(6.283185307179586 * u1);",
-     pins.pin_randn_special_angles),
-    ("randn half turn", "* cos(6.283185307179586 * u1);", "* cos(3.141592653589793 * u1);",
-     pins.pin_randn_special_angles),
+    ("randn sin branch", "return sqrt(-2.0 * log(1.0 - u0)) * cos(6.283185307179586 * u1);",
+     "return sqrt(-2.0 * log(1.0 - u0)) * sin(6.283185307179586 * u1);", pins.pin_randn_special_angles),
+    ("randn half turn", "return sqrt(-2.0 * log(1.0 - u0)) * cos(6.283185307179586 * u1);",
+     "return sqrt(-2.0 * log(1.0 - u0)) * cos(3.141592653589793 * u1);", pins.pin_randn_special_angles),
     ("randn swapped counters",
      "double u0 = (double)orc_uniform_f32(seed, 2u * counter);",
      "double u0 = (double)orc_uniform_f32(seed, 2u * counter + 1u);",
      pins.pin_randn_special_angles),
-    ("randn log(u)", "sqrt(-2.0 * log(1.0 - u0))", "sqrt(-2.0 * log(u0 + 0x1p-24))",
-     pins.pin_randn_special_angles),
+    ("randn log(u)", "return sqrt(-2.0 * log(1.0 - u0)) * cos(6.283185307179586 * u1);",
+     "return sqrt(-2.0 * log(u0 + 0x1p-24)) * cos(6.283185307179586 * u1);", pins.pin_randn_special_angles),
     ("paired sine for cosine", "return (counter & 1u) ? r * sin(6.283185307179586 * u1) : r * cos(6.283185307179586 * u1);",
      "return (counter & 1u) ? r * cos(6.283185307179586 * u1) : r * sin(6.283185307179586 * u1);",
      pins.pin_randn_paired),
