@@ -107,6 +107,10 @@ def next_specs():
     return [
         F("normal_f32_pairs", "float32", 4, 0, "fill_kernel<GenNormalF32Pairs>", "normal_f32.cu",
           lambda r, o, f, s: r.rng_fill_normal_f32_pairs(W.NORMAL_SEED, f, o, s)),
+        F("exponential_f32", "float32", 4, 0, "fill_kernel<GenExpF32>", "exponential.cu",
+          lambda r, o, f, s: r.rng_fill_exponential_f32(W.NORMAL_SEED, f, o, s)),
+        F("exponential_f64", "float64", 8, 0, "fill_kernel<GenExpF64>", "exponential.cu",
+          lambda r, o, f, s: r.rng_fill_exponential_f64(W.NORMAL_SEED, f, o, s)),
         F("u8", "uint8", 1, 0, "fill_kernel<GenU8>", "fill_narrow.cu",
           lambda r, o, f, s: r.rng_fill_u8(W.UNIFORM_SEED, f, o, s)),
         F("u16", "int16", 2, 0, "fill_kernel<GenU16>", "fill_narrow.cu",
@@ -401,7 +405,8 @@ def run_ours(args):
     if not args.no_next and not args.only:
         next_rows = {}
         views = {"uint8": buf4.view(torch.uint8), "int16": buf4.view(torch.int16),
-                 "float16": buf4.view(torch.float16), "bool": buf4.view(torch.bool), "float32": outs["float32"]}
+                 "float16": buf4.view(torch.float16), "bool": buf4.view(torch.bool), "float32": outs["float32"],
+                 "float64": outs["float64"]}
         for spec in next_specs():
             out = views[spec.kind][:n]
             for _ in range(3):

@@ -47,6 +47,8 @@ _FILL_SIGS = {
     "rng_fill_i64_range": [_u32, _u32, _sz, _i64, _u64, _p, _p],
     "rng_fill_normal_f32": [_u32, _u32, _sz, _p, _p],
     "rng_fill_normal_f32_pairs": [_u32, _u32, _sz, _p, _p],
+    "rng_fill_exponential_f32": [_u32, _u32, _sz, _p, _p],
+    "rng_fill_exponential_f64": [_u32, _u32, _sz, _p, _p],
     "rng_fill_normal_f64": [_u32, _u32, _sz, _p, _p],
     "rng_fill_normal_f64_noalloc": [_u32, _u32, _sz, _p, _p],
     "rng_dropout_fwd": [_p, _p, _f32, _u32, _u32, _sz, _p],
@@ -177,6 +179,14 @@ def rng_fill_normal_f32(seed, first_counter, out, stream=None):
 
 def rng_fill_normal_f32_pairs(seed, first_counter, out, stream=None):
     return _fill("rng_fill_normal_f32_pairs", "f32", seed, first_counter, out, stream)
+
+
+def rng_fill_exponential_f32(seed, first_counter, out, stream=None):
+    return _fill("rng_fill_exponential_f32", "f32", seed, first_counter, out, stream)
+
+
+def rng_fill_exponential_f64(seed, first_counter, out, stream=None):
+    return _fill("rng_fill_exponential_f64", "f64", seed, first_counter, out, stream)
 
 
 def rng_fill_normal_f64(seed, first_counter, out, stream=None):

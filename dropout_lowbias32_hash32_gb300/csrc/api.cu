@@ -268,6 +268,22 @@ rng_status rng_fill_normal_f32_pairs(uint32_t seed, uint32_t first_counter, size
     });
 }
 
+rng_status rng_fill_exponential_f32(uint32_t seed, uint32_t first_counter, size_t n, float *out, void *stream)
+{
+    const uint32_t key = seed_key(seed);
+    return fill("rng_fill_exponential_f32", first_counter, n, out, [&](uint32_t c, uint32_t len, float *o) {
+        return launch_fill_exponential_f32(key, c, len, o, RNG_STREAM(stream));
+    });
+}
+
+rng_status rng_fill_exponential_f64(uint32_t seed, uint32_t first_counter, size_t n, double *out, void *stream)
+{
+    const uint32_t key = seed_key(seed);
+    return fill("rng_fill_exponential_f64", first_counter, n, out, [&](uint32_t c, uint32_t len, double *o) {
+        return launch_fill_exponential_f64(key, c, len, o, RNG_STREAM(stream));
+    });
+}
+
 rng_status rng_fill_normal_f64(uint32_t seed, uint32_t first_counter, size_t n, double *out, void *stream)
 {
     return fill("rng_fill_normal_f64", first_counter, n, out, [&](uint32_t c, uint32_t len, double *o) {

@@ -77,6 +77,8 @@ cudaError_t launch_fill_i64_range(const Below64Args &a, int64_t low, uint32_t fi
 
 cudaError_t launch_fill_normal_f32(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
 cudaError_t launch_fill_normal_f32_pairs(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
+cudaError_t launch_fill_exponential_f32(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
+cudaError_t launch_fill_exponential_f64(uint32_t key, uint32_t first, uint32_t n, double *out, cudaStream_t s);
 
 // Dropout of one piece: keep iff (D32 & 0x7FFFFF) >= threshold, y = x / divisor.
 cudaError_t launch_dropout(const float *x, float *y, uint32_t key, uint32_t threshold, float divisor,

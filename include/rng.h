@@ -188,6 +188,21 @@ rng_status rng_fill_normal_f64(uint32_t seed, uint32_t first_counter, size_t n, 
 rng_status rng_fill_normal_f64_noalloc(uint32_t seed, uint32_t first_counter, size_t n, double *out,
                                        void *stream);
 
+/* ---- exponentials (tandem-sycl "Design", section Exponentials) ------------ */
+
+/* out[i] = -ln(1 - u), u = uniform(seed, c_i): 1 - u exact in (0, 1], within
+ * 2 ulp of the exact value, in [0, 23 ln 2]. */
+rng_status rng_fill_exponential_f32(uint32_t seed, uint32_t first_counter, size_t n, float *out,
+                                    void *stream);
+
+/* out[i] = 0 - zlog(1 - u), u = (D64(seed, c_i) >> 11) 2^-53: 1 - u exact, zlog
+ * the library's own logarithm (x = 2^e m, m in (sqrt(1/2), sqrt 2], the atanh
+ * series to s^23; the same fixed IEEE operations as the normal_f64 tail), so
+ * the value is reproducible bit for bit and within 2 ulp of -ln(1 - u); in
+ * [0, 53 ln 2].  FP64-bound on GB300 (about 26 FP64 operations per element). */
+rng_status rng_fill_exponential_f64(uint32_t seed, uint32_t first_counter, size_t n, double *out,
+                                    void *stream);
+
 /* ---- dropout (Phobos "Random numbers", section dropout) ------------------- */
 
 /* y[i] = uniform(seed, c_i) >= p ? x[i] / (1 - p) : +0, in f32 with IEEE

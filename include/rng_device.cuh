@@ -8,7 +8,8 @@
 //   draw32(k, c) = hash32(c ^ hash32(seed))             (section uniform);
 //   uniform      = (draw32 & 0x7FFFFF) * 2^-23         (section uniform);
 //   randn        = sqrt(-2 ln(1 - u(2c))) cos(2 pi u(2c + 1))  (section randn);
-//   dropout      = uniform >= p ? x / (1 - p) : 0       (section dropout).
+//   dropout      = uniform >= p ? x / (1 - p) : 0       (section dropout);
+//   exponential  = -ln(1 - uniform)  (tandem-sycl "Design", section Exponentials).
 // A kernel that gives element e the counter first + e draws exactly what
 // the corresponding fill writes: dropout() is bit-identical to
 // rng_dropout_fwd, uniform() to rng_fill_f32, draw32() to rng_fill_u32;
@@ -167,6 +168,17 @@ __device__ __forceinline__ float randn_paired(Key k, uint32_t c)
 {
     const float2 v = randn_pair(k, c >> 1);
     return (c & 1u) ? v.y : v.x;
+}
+
+// ---- exponential ----------------------------------------------------------------
+
+// -ln(1 - u) for u = uniform(k, c): 1 - u = 2 - (1 + u) exactly, CUDA's logf
+// (within 1 ulp), so the value is within 2 ulp of the exact one; 0 - ln
+// keeps u = 0 at +0.
+__device__ __forceinline__ float exponential(Key k, uint32_t c)
+{
+    const float one_minus_u = 2.0f - __uint_as_float(0x3F800000u | (draw32(k, c) & 0x7FFFFFu));
+    return 0.0f - logf(one_minus_u);
 }
 
 // ---- dropout ------------------------------------------------------------------

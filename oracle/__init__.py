@@ -74,6 +74,8 @@ _SIGS = {
     "orc_fill_i64_range": (None, [_u32, _u32, _sz, _p, _i64, _u64, _p]),
     "orc_fill_randn": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_fill_randn_paired": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_exponential_f32": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_exponential_f64": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_randn_paired": (_f64, [_u32, _u32]),
     "orc_fill_normal_f64": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_dropout_fill": (None, [_p, _f32, _u32, _u32, _sz, _p, _p]),
@@ -231,6 +233,13 @@ class Oracle:
     def fill_randn_paired(self, seed, first, n=None, idx=None):
         """binary64 values of the paired Box-Muller definition."""
         return self._fill("orc_fill_randn_paired", np.float64, seed, first, n, idx)
+
+    def fill_exponential_f32(self, seed, first, n=None, idx=None):
+        """binary64 values of -ln(1 - u) on the f32 uniform (not rounded to f32)."""
+        return self._fill("orc_fill_exponential_f32", np.float64, seed, first, n, idx)
+
+    def fill_exponential_f64(self, seed, first, n=None, idx=None):
+        return self._fill("orc_fill_exponential_f64", np.float64, seed, first, n, idx)
 
     def fill_normal_f64(self, seed, first, n=None, idx=None):
         return self._fill("orc_fill_normal_f64", np.float64, seed, first, n, idx)

@@ -335,6 +335,23 @@ double orc_zlog(double x)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Exponentials [Tandem-D, section Exponentials]: -ln(1 - u).  READING: the   */
+/* f32 fill on the f32 uniform (evaluated here in binary64, not rounded), the */
+/* f64 fill on the f64 uniform through this file's own logarithm.            */
+/* ------------------------------------------------------------------------ */
+
+double orc_exponential_f32(uint32_t seed, uint32_t counter)
+{
+    return -log(1.0 - (double)orc_uniform_f32(seed, counter));
+}
+
+double orc_exponential_f64(uint32_t seed, uint32_t counter)
+{
+    double v = 1.0 - orc_uniform_f64(seed, counter);
+    return 0.0 - orc_zlog(v);
+}
+
+/* ------------------------------------------------------------------------ */
 /* 1024-layer Marsaglia-Tsang ziggurat [Tandem-D, section Normals]           */
 /* (Marsaglia & Tsang 2000, "The Ziggurat Method for Generating Random       */
 /* Variables").                                                              */
@@ -577,6 +594,16 @@ void orc_fill_randn(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx
 void orc_fill_randn_paired(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)
 {
     for (size_t i = 0; i < n; ++i) out[i] = orc_randn_paired(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_exponential_f32(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_exponential_f32(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_exponential_f64(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_exponential_f64(seed, counter_of(first, idx, i));
 }
 
 void orc_fill_normal_f64(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)

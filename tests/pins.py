@@ -210,9 +210,16 @@ def pin_ranges_wrap(orc):
 
 
 # ------------------------------------------------------------------ randn --
+_LOW23_CACHE = {}
+
+
 def _counters_with_low23(orc, seed: int, word: int, targets, first_n: int = 1 << 26):
     """Counters c (< first_n / 2) whose uniform at 2c + word has the given 23-bit grid index."""
-    d = orc.fill_u32(seed, word, first_n)[::2] & 0x7FFFFF
+    key = (id(orc), seed, word, first_n)
+    if key not in _LOW23_CACHE:
+        _LOW23_CACHE.clear()
+        _LOW23_CACHE[key] = orc.fill_u32(seed, word, first_n)[::2] & 0x7FFFFF
+    d = _LOW23_CACHE[key]
     return {t: np.nonzero(d == t)[0] for t in targets}
 
 
@@ -292,6 +299,32 @@ def pin_randn_paired(orc):
     assert np.allclose(zq, rq, rtol=1e-14, atol=0)
     _normal_stats(y)
     assert abs(np.corrcoef(x, y)[0, 1]) < 5 / math.sqrt(n)
+
+
+def pin_exponentials(orc):
+    """-ln(1 - u): at u = 0 the value is +0 and at the top of the 2^-23 grid
+    23 ln 2; the f64 fill is within 2 ulp of numpy's -log1p(-u) on the exact
+    f64 uniform; both have mean 1, variance 1 and pass a 200-bin chi-square
+    against 1 - exp(-x)."""
+    n = 1 << 21
+    u = orc.fill_f32(13, 0, n).astype(np.float64)
+    e = orc.fill_exponential_f32(13, 0, n)
+    assert np.allclose(e, -np.log1p(-u), rtol=1e-15, atol=0)
+    hits = _counters_with_low23(orc, 7, 0, (0, (1 << 23) - 1))
+    c0, ctop = 2 * hits[0][:4], 2 * hits[(1 << 23) - 1][:4]
+    assert c0.size and ctop.size
+    assert np.all(orc.fill_exponential_f32(7, 0, idx=c0) == 0)
+    assert np.allclose(orc.fill_exponential_f32(7, 0, idx=ctop), 23 * math.log(2), rtol=1e-15)
+    u64 = orc.fill_f64(13, 0, n)
+    e64 = orc.fill_exponential_f64(13, 0, n)
+    ref = -np.log1p(-u64)
+    nz = ref > 0
+    assert _ulps(e64[nz], ref[nz]).max() <= 2
+    assert np.all(e64[~nz] == 0) and not np.any(np.signbit(e64))
+    edges = np.append(-np.log1p(-np.linspace(0, 1, 201)[:-1]), np.inf)
+    for x in (e, e64):
+        assert abs(x.mean() - 1) < 5 / math.sqrt(n) and abs(x.var() - 1) < 5 * math.sqrt(8 / n)
+        assert stats.chisquare(np.histogram(x, bins=edges)[0]).pvalue > 1e-3
 
 
 # ---------------------------------------------------------------- dropout --
@@ -452,6 +485,8 @@ def pin_slice_invariant(orc):
         lambda f, m, idx=None: orc.fill_bool(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_f16_bits(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_randn_paired(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_exponential_f32(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_exponential_f64(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_u32(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_u64(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_f32(9, f, m, idx),
@@ -479,7 +514,7 @@ ALL_PINS = [
     pin_tile_mean, pin_uniform_grid, pin_hash_bijective, pin_draw64_words, pin_narrow_fills,
     pin_lemire_exhaustive_8bit, pin_lemire_exhaustive_16bit, pin_lemire_wide_words,
     pin_below_distributions, pin_ranges_wrap, pin_randn_special_angles,
-    pin_randn_tail_end, pin_randn_distribution, pin_randn_paired, pin_dropout, pin_zexp_zlog,
+    pin_randn_tail_end, pin_randn_distribution, pin_randn_paired, pin_exponentials, pin_dropout, pin_zexp_zlog,
     pin_zig_table_published, pin_zig_table_invariants, pin_zig_miss_rate,
     pin_normal_f64_distribution, pin_zig_wedge_acceptance, pin_slice_invariant,
 ]

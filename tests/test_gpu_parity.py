@@ -94,6 +94,8 @@ def fills(rng, torch, orc):
                       lambda f, n: orc.fill_i64_range(4, f, -500, 1000, n)),
         "normal_f64": (lambda o, f: rng.rng_fill_normal_f64(7, f, o), t.float64,
                        lambda f, n: orc.fill_normal_f64(7, f, n)),
+        "exponential_f64": (lambda o, f: rng.rng_fill_exponential_f64(13, f, o), t.float64,
+                            lambda f, n: orc.fill_exponential_f64(13, f, n)),
         "u8": (lambda o, f: rng.rng_fill_u8(0x9E3779B9, f, o), t.uint8,
                lambda f, n: orc.fill_u8(0x9E3779B9, f, n)),
         "u16": (lambda o, f: rng.rng_fill_u16(0x9E3779B9, f, o), t.int16,
@@ -107,7 +109,7 @@ def fills(rng, torch, orc):
 
 FILL_NAMES = ["u32", "u64", "f32", "f64", "u32_below_1000", "u32_below_2^32-2", "u32_below_2^31+1",
               "u64_below_1000", "u64_below_2^64-2", "u64_below_2^63+1", "i32_range", "i32_range_wrap",
-              "i64_range32", "i64_range", "normal_f64", "u8", "u16", "f16", "bool"]
+              "i64_range32", "i64_range", "normal_f64", "u8", "u16", "f16", "bool", "exponential_f64"]
 
 
 @pytest.mark.parametrize("name", FILL_NAMES)
@@ -190,6 +192,18 @@ def test_normal_f32_pairs_within_tolerance(rng, torch, orc):
     pairs = _host(rng.rng_fill_normal_f32_pairs(9, 0, _out(torch, torch.float32, 20000, 0)))
     cos_branch = _host(rng.rng_fill_normal_f32(9, 0, _out(torch, torch.float32, 10000, 0)))
     assert np.array_equal(pairs[0::2].view(np.uint32), cos_branch.view(np.uint32))
+
+
+def test_exponential_f32_within_two_ulp(rng, torch, orc):
+    """-ln(1 - u) in f32 within 2 ulp of the oracle's binary64 value (at u = 0
+    exactly +0)."""
+    for first, n, offset in ((0, 1 << 22, 0), (1, 4099, 1), (U32 - 5, BIG, 3)):
+        e = _host(rng.rng_fill_exponential_f32(13, first, _out(torch, torch.float32, n, offset)))
+        ref = orc.fill_exponential_f32(13, first, n)
+        ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+        err = np.abs(e.astype(np.float64) - ref)
+        assert np.all(err <= 2 * ulp), (first, n, np.max(err / ulp))
+        assert not np.any(np.signbit(e))
 
 
 @pytest.mark.parametrize("p", [0.1, 0.5, 0.0, 0.999, 2.0 ** -30])

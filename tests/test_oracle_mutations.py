@@ -50,6 +50,9 @@ MUTATIONS = [
      "return (counter & 1u) ? r * cos(6.283185307179586 * u1) : r * sin(6.283185307179586 * u1);",
      pins.pin_randn_paired),
     ("paired pair index", "    uint32_t q = counter >> 1;", "    uint32_t q = (counter + 1u) >> 1;", pins.pin_randn_paired),
+    ("exponential f32 of u", "return -log(1.0 - (double)orc_uniform_f32(seed, counter));",
+     "return -log((double)orc_uniform_f32(seed, counter) + 0x1p-24);", pins.pin_exponentials),
+    ("exponential f64 sign", "return 0.0 - orc_zlog(v);", "return orc_zlog(v);", pins.pin_exponentials),
     ("dropout drops ties", "return (u >= p) ? x / keep_scale_divisor : 0.0f;",
      "return (u > p) ? x / keep_scale_divisor : 0.0f;", pins.pin_dropout),
     ("dropout reciprocal multiply", "return (u >= p) ? x / keep_scale_divisor : 0.0f;",
