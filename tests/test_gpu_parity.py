@@ -345,3 +345,43 @@ def test_bad_arguments_raise(rng, torch):
         rng.rng_dropout_fwd(o[:6], o[2:8], 0.5, 1, 0)
     with pytest.raises(TypeError):
         rng.rng_fill_u32(1, 0, torch.empty(8, dtype=torch.int32))
+
+
+def test_degenerate_bounds(rng, torch, orc):
+    """bound 1 gives zeros; the largest bounds (2^32 - 1, 2^64 - 1) reject
+    almost nothing and still match the oracle bit for bit."""
+    n = 70001
+    out32 = torch.empty(n, dtype=torch.int32, device="cuda")
+    out64 = torch.empty(n, dtype=torch.int64, device="cuda")
+    assert not bool(rng.rng_fill_u32_below(1, 5, 1, out32).any())
+    assert not bool(rng.rng_fill_u64_below(1, 5, 1, out64).any())
+    for b in (2, U32 - 1):
+        _assert_equal(f"u32_below {b}", _host(rng.rng_fill_u32_below(6, U32 - 3, b, out32)),
+                      orc.fill_u32_below(6, U32 - 3, b, n).view(np.int32))
+    for b in (2, (1 << 64) - 1, 1 << 63):
+        _assert_equal(f"u64_below {b}", _host(rng.rng_fill_u64_below(6, U32 - 3, b, out64)),
+                      orc.fill_u64_below(6, U32 - 3, b, n).view(np.int64))
+    lo = -(1 << 63)
+    _assert_equal("i64_range extremes", _host(rng.rng_fill_i64_range(6, 1, lo, (1 << 64) - 1, out64)),
+                  orc.fill_i64_range(6, 1, lo, (1 << 64) - 1, n))
+
+
+def test_dropout_largest_p_drops_everything(rng, torch, orc):
+    p = float(np.nextafter(np.float32(1), np.float32(0)))  # 1 - 2^-24
+    x = workloads.dropout_x(4099)
+    y = rng.rng_dropout_fwd(torch.from_numpy(x).cuda(), torch.empty(4099, device="cuda"), p, 42, 0)
+    assert np.all(_host(y).view(np.uint32) == 0)
+    _assert_equal("p max", _host(y), orc.dropout(x, p, 42, 0))
+
+
+def test_fill_longer_than_the_counter_period(rng, torch, orc):
+    """n > 2^32 elements: counters wrap inside one call, so element i + 2^32
+    repeats element i (u8 fill: 4 GiB)."""
+    n = (1 << 32) + 1000
+    out = rng.rng_fill_u8(5, 7, torch.empty(n, dtype=torch.uint8, device="cuda"))
+    head = _host(out[:1000])
+    assert np.array_equal(_host(out[1 << 32:]), head)
+    idx = np.concatenate([np.arange(1000), np.random.default_rng(3).integers(0, n, 1 << 16)])
+    _assert_equal("u8 > 2^32", _host(out[torch.from_numpy(idx).cuda()]), orc.fill_u8(5, 7, idx=idx))
+    del out
+    torch.cuda.empty_cache()
