@@ -12,11 +12,13 @@
 // 1 - p rounded to f32 on the host.  Dropped elements are +0.  The element
 // function is lowbias32::dropout of include/rng_device.cuh.
 //
-// When x and y share their offset within 16 bytes, every thread moves one
-// 16-byte vector in and one out (warps read and write 512 contiguous bytes);
-// otherwise a scalar grid-stride kernel keeps both sides coalesced.  x == y
-// (in place) is fine: each element is read before it is written by the same
-// thread, so neither pointer is declared __restrict__.
+// When x and y share their offset within 16 bytes, every thread moves
+// kFillVectorsPerThread 16-byte vectors in and out (warps read and write 512
+// contiguous bytes per instruction; block b owns the b-th contiguous run of
+// kFillThreads x kFillVectorsPerThread vectors, its loads issued before its
+// stores); otherwise a scalar kernel of the same chunked shape keeps both
+// sides coalesced.  x == y (in place) is fine: each element is read before it
+// is written by the same thread, so neither pointer is declared __restrict__.
 #include "fill_kernel.cuh"
 #include "hash32.cuh"
 
@@ -28,12 +30,22 @@ __device__ __forceinline__ float drop(float x, uint32_t key, uint32_t threshold,
     return lowbias32::dropout(lowbias32::Dropout{lowbias32::Key{key}, threshold, divisor}, x, c);
 }
 
+__device__ __forceinline__ float4 drop4(float4 a, uint32_t key, uint32_t threshold, float divisor, uint32_t c)
+{
+    return make_float4(drop(a.x, key, threshold, divisor, c), drop(a.y, key, threshold, divisor, c + 1u),
+                       drop(a.z, key, threshold, divisor, c + 2u), drop(a.w, key, threshold, divisor, c + 3u));
+}
+
+constexpr uint32_t kVpt = kFillVectorsPerThread;
+// elements per thread of the scalar kernel (the same bytes per block as the
+// vector kernel)
+constexpr uint32_t kEpt = 4u * kFillVectorsPerThread;
+
 __global__ void __launch_bounds__(kFillThreads)
 dropout_vec_kernel(const float *x, float *y, uint32_t key, uint32_t threshold, float divisor, uint32_t first,
                    uint32_t head, uint32_t n_vec, uint32_t n)
 {
     const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
-    const uint32_t stride = gridDim.x * blockDim.x;
     const uint32_t tail0 = head + n_vec * 4u;
     if (tid < head) y[tid] = drop(x[tid], key, threshold, divisor, first + tid);
     if (tid < n - tail0) y[tail0 + tid] = drop(x[tail0 + tid], key, threshold, divisor, first + tail0 + tid);
@@ -41,15 +53,24 @@ dropout_vec_kernel(const float *x, float *y, uint32_t key, uint32_t threshold, f
     const float4 *xv = reinterpret_cast<const float4 *>(x + head);
     float4 *yv = reinterpret_cast<float4 *>(y + head);
     const uint32_t c0 = first + head;
-    for (uint32_t v = tid; v < n_vec; v += stride) {
-        const float4 a = __ldcs(xv + v);
-        const uint32_t c = c0 + 4u * v;
-        float4 b;
-        b.x = drop(a.x, key, threshold, divisor, c);
-        b.y = drop(a.y, key, threshold, divisor, c + 1u);
-        b.z = drop(a.z, key, threshold, divisor, c + 2u);
-        b.w = drop(a.w, key, threshold, divisor, c + 3u);
-        __stcs(yv + v, b);
+    const uint32_t block0 = blockIdx.x * (kFillThreads * kVpt);
+    const uint32_t v0 = block0 + threadIdx.x;
+    // block0 <= n_vec for every block of chunk_blocks' grid, so no wrap
+    if (n_vec - block0 >= kFillThreads * kVpt) {
+        float4 a[kVpt];
+#pragma unroll
+        for (uint32_t j = 0; j < kVpt; ++j) a[j] = __ldcs(xv + v0 + j * kFillThreads);
+#pragma unroll
+        for (uint32_t j = 0; j < kVpt; ++j) {
+            const uint32_t v = v0 + j * kFillThreads;
+            __stcs(yv + v, drop4(a[j], key, threshold, divisor, c0 + 4u * v));
+        }
+    } else {
+#pragma unroll
+        for (uint32_t j = 0; j < kVpt; ++j) {
+            const uint32_t v = v0 + j * kFillThreads;
+            if (v < n_vec) __stcs(yv + v, drop4(__ldcs(xv + v), key, threshold, divisor, c0 + 4u * v));
+        }
     }
 }
 
@@ -57,9 +78,25 @@ __global__ void __launch_bounds__(kFillThreads)
 dropout_scalar_kernel(const float *x, float *y, uint32_t key, uint32_t threshold, float divisor,
                       uint32_t first, uint32_t n)
 {
-    const uint32_t stride = gridDim.x * blockDim.x;
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-        y[i] = drop(__ldcs(x + i), key, threshold, divisor, first + i);
+    const uint32_t block0 = blockIdx.x * (kFillThreads * kEpt);
+    const uint32_t i0 = block0 + threadIdx.x;
+    // block0 <= n for every block of chunk_blocks' grid, so no wrap
+    if (n - block0 >= kFillThreads * kEpt) {
+        float a[kEpt];
+#pragma unroll
+        for (uint32_t j = 0; j < kEpt; ++j) a[j] = __ldcs(x + i0 + j * kFillThreads);
+#pragma unroll
+        for (uint32_t j = 0; j < kEpt; ++j) {
+            const uint32_t i = i0 + j * kFillThreads;
+            y[i] = drop(a[j], key, threshold, divisor, first + i);
+        }
+    } else {
+#pragma unroll
+        for (uint32_t j = 0; j < kEpt; ++j) {
+            const uint32_t i = i0 + j * kFillThreads;
+            if (i < n) y[i] = drop(__ldcs(x + i), key, threshold, divisor, first + i);
+        }
+    }
 }
 
 }  // namespace
@@ -71,11 +108,11 @@ cudaError_t launch_dropout(const float *x, float *y, uint32_t key, uint32_t thre
     if ((ax & 15u) == (ay & 15u)) {
         const uint32_t head = head_elems<float>(y, n);
         const uint32_t n_vec = (n - head) / 4u;
-        dropout_vec_kernel<<<fill_blocks(n_vec), kFillThreads, 0, s>>>(x, y, key, threshold, divisor, first,
+        dropout_vec_kernel<<<chunk_blocks(n_vec, kVpt), kFillThreads, 0, s>>>(x, y, key, threshold, divisor, first,
                                                                        head, n_vec, n);
     } else {
-        dropout_scalar_kernel<<<fill_blocks((n + 3u) / 4u), kFillThreads, 0, s>>>(x, y, key, threshold,
-                                                                                  divisor, first, n);
+        dropout_scalar_kernel<<<chunk_blocks(n, kEpt), kFillThreads, 0, s>>>(x, y, key, threshold, divisor,
+                                                                              first, n);
     }
     note_launch();
     return cudaGetLastError();

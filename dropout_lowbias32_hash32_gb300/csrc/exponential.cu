@@ -22,7 +22,6 @@ namespace {
 
 struct GenExpF32 {
     using T = float;
-    static constexpr uint32_t kVectorsPerStep = 2;
     uint32_t key;
     __device__ T operator()(uint32_t c) const { return lowbias32::exponential(lowbias32::Key{key}, c); }
 };

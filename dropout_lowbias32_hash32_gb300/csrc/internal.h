@@ -11,7 +11,10 @@ namespace rngk {
 
 // Threads per block of the streaming fill kernels.
 constexpr unsigned kFillThreads = 256;
-// Resident blocks per SM the grid-stride fills aim for (2048 threads / SM).
+// 16-byte vectors each thread of a chunked fill writes (block b writes the
+// b-th run of kFillThreads x kFillVectorsPerThread vectors).
+constexpr unsigned kFillVectorsPerThread = 4;
+// Resident blocks per SM of the grid-stride kernels (2048 threads / SM).
 constexpr unsigned kFillBlocksPerSm = 8;
 // Largest number of elements one launch covers; the C ABI splits longer
 // fills into pieces of at most this size (a fill cut anywhere equals the
