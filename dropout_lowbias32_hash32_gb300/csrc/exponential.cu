@@ -22,6 +22,7 @@ namespace {
 
 struct GenExpF32 {
     using T = float;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     uint32_t key;
     __device__ T operator()(uint32_t c) const { return lowbias32::exponential(lowbias32::Key{key}, c); }
 };
@@ -41,6 +42,7 @@ __device__ __forceinline__ double u53_exact(Words w)
 
 struct GenExpF64 {
     using T = double;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     uint32_t key;
     __device__ T operator()(uint32_t c) const
     {

@@ -66,12 +66,14 @@ __device__ __forceinline__ uint64_t below64(const Below64Args &a, uint32_t c)
 
 struct GenBelow32 {
     using T = uint32_t;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     Below32Args a;
     __device__ T operator()(uint32_t c) const { return below32(a, c); }
 };
 
 struct GenBelow64 {
     using T = uint64_t;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     Below64Args a;
     __device__ T operator()(uint32_t c) const { return below64(a, c); }
 };
@@ -80,6 +82,7 @@ struct GenBelow64 {
 // bit pattern reinterpreted).
 struct GenI32Range {
     using T = int32_t;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     Below32Args a;
     int32_t low;
     __device__ T operator()(uint32_t c) const
@@ -100,6 +103,7 @@ struct GenI64Range32 {
 
 struct GenI64Range {
     using T = int64_t;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     Below64Args a;
     int64_t low;
     __device__ T operator()(uint32_t c) const

@@ -91,6 +91,7 @@ __device__ __forceinline__ uint32_t f16_pair(uint32_t two_halfwords)
 
 struct GenF16 {
     using T = uint16_t;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     uint32_t key;
     __device__ T operator()(uint32_t c) const
     {

@@ -61,6 +61,7 @@ __device__ __forceinline__ double scaled_u53_to_double(Words w)
 
 struct GenF64 {
     using T = double;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     uint32_t key;
     __device__ T operator()(uint32_t c) const { return scaled_u53_to_double(draw64_words(key, c)); }
 };

@@ -14,6 +14,10 @@ constexpr unsigned kFillThreads = 256;
 // 16-byte vectors each thread of a chunked fill writes (block b writes the
 // b-th run of kFillThreads x kFillVectorsPerThread vectors).
 constexpr unsigned kFillVectorsPerThread = 4;
+// The same for generators of many instructions per element (bounded
+// integers, f64 and f16 uniforms, normals, exponentials), which gain from
+// more independent vectors in flight per thread.
+constexpr unsigned kHeavyVectorsPerThread = 8;
 // Resident blocks per SM of the grid-stride kernels (2048 threads / SM).
 constexpr unsigned kFillBlocksPerSm = 8;
 // Largest number of elements one launch covers; the C ABI splits longer

@@ -18,6 +18,7 @@ namespace {
 
 struct GenNormalF32 {
     using T = float;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     uint32_t key;  // folded hash of the seed
     __device__ T operator()(uint32_t c) const { return lowbias32::randn(lowbias32::Key{key}, c); }
 };
@@ -30,6 +31,7 @@ struct GenNormalF32 {
 // an odd start needs three pairs per vector instead of two.
 struct GenNormalF32Pairs {
     using T = float;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     uint32_t key;
     __device__ T operator()(uint32_t c) const { return lowbias32::randn_paired(lowbias32::Key{key}, c); }
     __device__ Vec16<float> vec(uint32_t c0) const
