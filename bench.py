@@ -363,6 +363,8 @@ def run_ours(args):
     value = written * world * args.steps / (elapsed_ms / 1e3) / GIB
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["hbm_gbs"])
+    ceiling = write_ceiling(rng, torch, buf4, stream, max(args.steps, 5))
+    wpeak = max(ceiling["memset_gb_s"], ceiling["store_v4_gb_s"])
     fills = {}
     for s in specs:
         ms = fill_ms[s.name]
@@ -370,6 +372,8 @@ def run_ours(args):
         fills[s.name] = {"ms": round(ms, 4), "gib_s_written": round(s.written * n / (ms / 1e3) / GIB, 1),
                          "gb_s_traffic": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 3),
                          "kernel": s.kernel}
+        if s.read == 0:
+            fills[s.name]["frac_of_write_ceiling"] = round(gbs / wpeak, 3)
 
     # the kernel with the largest share of the step, over all of its calls
     by_kernel = {}
@@ -421,7 +425,8 @@ def run_ours(args):
             ms = statistics.median(a.elapsed_time(b) for a, b in evs)
             gbs = spec.written * n / (ms / 1e3) / 1e9
             next_rows[spec.name] = {"ms": round(ms, 4), "gib_s_written": round(spec.written * n / (ms / 1e3) / GIB, 1),
-                                    "frac_of_hbm": round(gbs / peak, 3), "kernel": spec.kernel}
+                                    "frac_of_hbm": round(gbs / peak, 3),
+                                    "frac_of_write_ceiling": round(gbs / wpeak, 3), "kernel": spec.kernel}
 
     e2e = None
     if not args.no_e2e:
@@ -440,7 +445,7 @@ def run_ours(args):
                        "elements_per_fill": n, "fills_per_step": len(specs), "bytes_written_per_step": written,
                        "l2": "outputs of 1-2 GiB per fill exceed the 129 MB L2; no flush between steps",
                        "parallelism": f"counter-range shards x{world}"},
-            "fills": fills, "roofline": roofline, "slowest_fill": slow, "next_rows": next_rows, "e2e": e2e,
+            "fills": fills, "write_ceiling": ceiling, "roofline": roofline, "slowest_fill": slow, "next_rows": next_rows, "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clocks.summary(),
             "cpu_baseline": None if args.no_cpu else cpu_baseline(specs),
@@ -449,6 +454,25 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return result
+
+
+def write_ceiling(rng, torch, buf, stream, reps):
+    """The write ceiling measured live on this GPU, outside the timed region:
+    cudaMemsetAsync and the plainest 16-byte store kernel over the 4-byte
+    output buffer (median of reps event-timed calls after 3 untimed)."""
+    nbytes = buf.numel() * buf.element_size()
+    out = {"bytes": nbytes}
+    for which, key in ((0, "memset_gb_s"), (1, "store_v4_gb_s")):
+        for _ in range(3):
+            rng.rng_debug_write_ceiling(which, buf, stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in evs:
+            a.record(stream)
+            rng.rng_debug_write_ceiling(which, buf, stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        out[key] = round(nbytes / (statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3) / 1e9, 1)
+    return out
 
 
 def run_e2e(rng, torch, specs, outs, host_inputs, x, dy, n, stream, barrier, dist, dev, steps, world):

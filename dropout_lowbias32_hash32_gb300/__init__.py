@@ -56,6 +56,7 @@ _FILL_SIGS = {
     "rng_debug_set_miss_capacity": [_sz],
     "rng_debug_last_miss_count": [C.POINTER(_u64)],
     "rng_debug_eval_f64": [_int, _p, _p, _sz, _p],
+    "rng_debug_write_ceiling": [_int, _p, _sz, _p],
 }
 for _name, _args in _FILL_SIGS.items():
     _fn = getattr(_lib, _name)
@@ -237,6 +238,16 @@ def rng_debug_last_miss_count() -> int:
 
 def rng_debug_launch_count() -> int:
     return _lib.rng_debug_launch_count()
+
+
+def rng_debug_write_ceiling(which: int, buf, stream=None):
+    """which = 0: cudaMemsetAsync over buf; 1: the plain 16-byte store kernel."""
+    if not buf.is_contiguous():
+        raise ValueError("rng_debug_write_ceiling: buf must be contiguous")
+    nbytes = buf.numel() * buf.element_size()
+    _check(_lib.rng_debug_write_ceiling(which, buf.data_ptr(), nbytes, _stream(stream, buf)),
+           "rng_debug_write_ceiling")
+    return buf
 
 
 def rng_debug_eval_f64(which: int, inp, out, stream=None):

@@ -354,4 +354,23 @@ rng_status rng_debug_eval_f64(int which, const double *in, double *out, size_t n
     });
 }
 
+rng_status rng_debug_write_ceiling(int which, void *buf, size_t bytes, void *stream)
+{
+    if (which != 0 && which != 1) return fail(RNG_EINVAL, "rng_debug_write_ceiling: which must be 0 or 1");
+    if (bytes == 0) return RNG_OK;
+    if (buf == nullptr) return fail(RNG_EINVAL, "rng_debug_write_ceiling: buf is NULL with bytes = %zu", bytes);
+    t_error[0] = '\0';
+    if (which == 0) {
+        const cudaError_t e = cudaMemsetAsync(buf, 0x5A, bytes, RNG_STREAM(stream));
+        return e == cudaSuccess ? RNG_OK : fail(RNG_ECUDA, "rng_debug_write_ceiling: %s", cudaGetErrorString(e));
+    }
+    if (reinterpret_cast<uintptr_t>(buf) % 16 != 0 || bytes % 16 != 0)
+        return fail(RNG_EINVAL, "rng_debug_write_ceiling: the store kernel needs a 16-byte aligned buffer of "
+                                "whole 16-byte vectors");
+    uint4 *out = static_cast<uint4 *>(buf);
+    return for_pieces(bytes / 16, 0, "rng_debug_write_ceiling", [&](size_t off, uint32_t, uint32_t len) {
+        return launch_store_ceiling(out + off, len, RNG_STREAM(stream));
+    });
+}
+
 }  // extern "C"

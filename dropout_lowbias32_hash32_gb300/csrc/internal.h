@@ -103,4 +103,7 @@ cudaError_t launch_eval_f64(int which, const double *in, double *out, uint32_t n
 constexpr size_t kNoAllocMaxElements = size_t(1) << 28;
 cudaError_t launch_normal_f64_noalloc(uint32_t seed, uint32_t first, uint32_t n, double *out, cudaStream_t s);
 
+// Plain 16-byte stores of n_vec vectors (the write-ceiling measurement).
+cudaError_t launch_store_ceiling(uint4 *out, uint32_t n_vec, cudaStream_t s);
+
 }  // namespace rngk

@@ -249,6 +249,15 @@ uint64_t rng_debug_launch_count(void);
  * doubles.  For checking the slow path layer by layer. */
 rng_status rng_debug_eval_f64(int which, const double *in, double *out, size_t n, void *stream);
 
+/* A measurement aid with no counterpart on the pages: the write ceiling the
+ * fills are compared with.  which = 0 enqueues cudaMemsetAsync(buf, 0x5A,
+ * bytes); which = 1 launches the plainest 16-byte store kernel over buf, in
+ * the launch shape of the fills (buf 16-byte aligned, bytes a multiple of
+ * 16).  buf is a caller-owned device buffer whose contents are overwritten;
+ * stream-ordered on stream.  RNG_EINVAL for another which, buf == NULL with
+ * bytes > 0, or (which = 1) a misaligned buf or size; bytes == 0 is a no-op. */
+rng_status rng_debug_write_ceiling(int which, void *buf, size_t bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -95,6 +95,12 @@ def test_debug_hooks_without_gpu(rng):
     assert rng.raw("rng_debug_last_miss_count")(None) == rng.RNG_EINVAL
     assert rng.rng_debug_launch_count() >= 0
     rng.rng_debug_set_miss_capacity(None)
+    ceiling = rng.raw("rng_debug_write_ceiling")
+    assert ceiling(2, 0x1000, 16, None) == rng.RNG_EINVAL
+    assert ceiling(0, None, 16, None) == rng.RNG_EINVAL
+    assert ceiling(1, 0x1008, 16, None) == rng.RNG_EINVAL  # misaligned for the store kernel
+    assert ceiling(1, 0x1000, 24, None) == rng.RNG_EINVAL  # not whole 16-byte vectors
+    assert ceiling(1, 0x1000, 0, None) == rng.RNG_OK
 
 
 def test_python_names_match_c_names(rng):

@@ -319,6 +319,21 @@ def test_launch_counts(rng, torch):
     assert rng.rng_debug_launch_count() - before == 2
 
 
+@pytest.mark.gpu
+def test_write_ceiling_hook_writes_what_it_states(rng, torch):
+    """The measurement aid behind bench.py's write ceiling: the store kernel
+    writes vector index v to each word of 16-byte vector v, memset 0x5A bytes."""
+    n_vec = 3 * 1024 + 17  # several blocks' runs and a ragged last run
+    buf = torch.empty(n_vec * 4, dtype=torch.int32, device="cuda")
+    before = rng.rng_debug_launch_count()
+    rng.rng_debug_write_ceiling(1, buf)
+    assert rng.rng_debug_launch_count() - before == 1
+    got = _host(buf).view(np.uint32).reshape(n_vec, 4)
+    assert np.array_equal(got, np.repeat(np.arange(n_vec, dtype=np.uint32)[:, None], 4, axis=1))
+    rng.rng_debug_write_ceiling(0, buf)
+    assert np.all(_host(buf).view(np.uint8) == 0x5A)
+
+
 def test_fill_longer_than_one_piece(rng, torch, orc):
     """n > 2^31 is split into pieces of 2^31 elements; the seam is invisible."""
     n = (1 << 31) + 1000
