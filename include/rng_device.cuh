@@ -18,7 +18,8 @@
 // one seed disjoint counters (randn reads the uniforms at 2c and 2c + 1).
 //
 // Keys are made once on the host (make_key, make_dropout) and passed to the
-// kernel by value.  The header needs only <stdint.h> and nvcc.
+// kernel by value.  The header needs only <stdint.h> and nvcc.  It also holds
+// the page's dropout_rows tile kernel with its R autotuner.
 #pragma once
 
 #include <stdint.h>
@@ -211,5 +212,104 @@ __device__ __forceinline__ float dropout(const Dropout &d, float x, uint32_t c)
 {
     return dropout_keep(d, c) ? __fdiv_rn(x, d.divisor) : 0.0f;
 }
+
+// ---- the dropout_rows tile kernel ---------------------------------------------
+
+// Phobos "Random numbers", the dropout_rows listing: y = dropout(x) on a
+// [rows, 256] f32 tensor, a block of 256 threads (one column each) per R
+// rows, the counter of element (row, col) its flat index first + row 256 +
+// col (mod 2^32), so every R gives exactly what rng_dropout_fwd gives for
+// the flattened tensor.  Each thread loads its R elements before computing
+// and storing them.  x == y is allowed (each element is read before it is
+// written, by the same thread).
+constexpr uint32_t kDropoutRowsCols = 256;
+
+template <int R>
+__global__ void __launch_bounds__(kDropoutRowsCols)
+    dropout_rows_kernel(const float *x, float *y, uint32_t rows, Dropout d, uint32_t first)
+{
+    const uint32_t row0 = blockIdx.x * static_cast<uint32_t>(R);
+    const uint32_t col = threadIdx.x;
+    float v[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const size_t e = static_cast<size_t>(row0 + r) * kDropoutRowsCols + col;
+        if (row0 + r < rows) v[r] = x[e];
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const size_t e = static_cast<size_t>(row0 + r) * kDropoutRowsCols + col;
+        if (row0 + r < rows) y[e] = dropout(d, v[r], first + static_cast<uint32_t>(e));
+    }
+}
+
+#ifdef __CUDACC__
+// The candidate R (rows per block) the autotuner tries; the listing's own
+// candidate list is the single value 16.
+constexpr int kDropoutRowsCandidates[] = {1, 2, 4, 8, 16, 32};
+constexpr int kDropoutRowsNumCandidates = 6;
+
+// Launches dropout_rows_kernel<R> for a candidate R on stream s (rows <
+// 2^32 / R); cudaErrorInvalidValue for an R outside the candidates.  (A
+// function template only so that a translation unit that does not call it
+// instantiates none of the kernels.)
+template <class = void>
+inline cudaError_t dropout_rows(const float *x, float *y, uint32_t rows, const Dropout &d, uint32_t first, int R,
+                                cudaStream_t s = 0)
+{
+    if (rows == 0) return cudaSuccess;
+    const uint32_t blocks = (rows + static_cast<uint32_t>(R) - 1u) / static_cast<uint32_t>(R);
+    switch (R) {
+    case 1: dropout_rows_kernel<1><<<blocks, kDropoutRowsCols, 0, s>>>(x, y, rows, d, first); break;
+    case 2: dropout_rows_kernel<2><<<blocks, kDropoutRowsCols, 0, s>>>(x, y, rows, d, first); break;
+    case 4: dropout_rows_kernel<4><<<blocks, kDropoutRowsCols, 0, s>>>(x, y, rows, d, first); break;
+    case 8: dropout_rows_kernel<8><<<blocks, kDropoutRowsCols, 0, s>>>(x, y, rows, d, first); break;
+    case 16: dropout_rows_kernel<16><<<blocks, kDropoutRowsCols, 0, s>>>(x, y, rows, d, first); break;
+    case 32: dropout_rows_kernel<32><<<blocks, kDropoutRowsCols, 0, s>>>(x, y, rows, d, first); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+// The listing's @autotune: times every candidate R on the caller's buffers
+// (one untimed launch, then `reps` >= 1 launches between CUDA events on s,
+// which is synchronised) and returns the R of the least mean time, or 0 on a
+// CUDA error (then cudaGetLastError() or the returned launch status says
+// which).  y is overwritten, with the same values whatever R.  ms, if not
+// null, receives the mean milliseconds of each candidate, in the order of
+// kDropoutRowsCandidates.
+template <class = void>
+inline int dropout_rows_autotune(const float *x, float *y, uint32_t rows, const Dropout &d, uint32_t first,
+                                 cudaStream_t s = 0, int reps = 5, float *ms = nullptr)
+{
+    if (reps < 1) reps = 1;
+    cudaEvent_t ev[2];
+    if (cudaEventCreate(&ev[0]) != cudaSuccess) return 0;
+    if (cudaEventCreate(&ev[1]) != cudaSuccess) {
+        cudaEventDestroy(ev[0]);
+        return 0;
+    }
+    int best = 0;
+    float best_ms = 0.0f;
+    bool ok = true;
+    for (int k = 0; ok && k < kDropoutRowsNumCandidates; ++k) {
+        const int R = kDropoutRowsCandidates[k];
+        ok = dropout_rows(x, y, rows, d, first, R, s) == cudaSuccess && cudaEventRecord(ev[0], s) == cudaSuccess;
+        for (int i = 0; ok && i < reps; ++i) ok = dropout_rows(x, y, rows, d, first, R, s) == cudaSuccess;
+        float t = 0.0f;
+        ok = ok && cudaEventRecord(ev[1], s) == cudaSuccess && cudaEventSynchronize(ev[1]) == cudaSuccess &&
+             cudaEventElapsedTime(&t, ev[0], ev[1]) == cudaSuccess;
+        t /= static_cast<float>(reps);
+        if (ok && ms) ms[k] = t;
+        if (ok && (best == 0 || t < best_ms)) {
+            best = R;
+            best_ms = t;
+        }
+    }
+    cudaEventDestroy(ev[0]);
+    cudaEventDestroy(ev[1]);
+    return ok ? best : 0;
+}
+#endif  // __CUDACC__
 
 }  // namespace lowbias32

@@ -19,23 +19,6 @@ __global__ void draw_kernel(uint32_t seed, uint32_t first, uint32_t n, uint32_t 
     }
 }
 
-// The Phobos page's dropout_rows: R rows of 256 columns per block, the
-// counter of element (r, col) its flat index (r0 + r) * 256 + col.
-template <int R>
-__global__ void dropout_rows_kernel(const float *x, float *y, uint32_t rows, lowbias32::Dropout d)
-{
-    const uint32_t r0 = blockIdx.x * R;
-    const uint32_t col = threadIdx.x;  // 256 threads, one column each
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const uint32_t row = r0 + r;
-        if (row < rows) {
-            const uint32_t c = row * 256u + col;
-            y[c] = lowbias32::dropout(d, x[c], c);
-        }
-    }
-}
-
 }  // namespace
 
 extern "C" int device_api_draws(uint32_t seed, uint32_t first, uint32_t n, uint32_t *d32, uint64_t *d64, float *u,
@@ -45,10 +28,23 @@ extern "C" int device_api_draws(uint32_t seed, uint32_t first, uint32_t n, uint3
     return static_cast<int>(cudaDeviceSynchronize());
 }
 
-extern "C" int device_api_dropout_rows(const float *x, float *y, uint32_t rows, uint32_t seed, float p)
+// The header's dropout_rows with rows-per-block R (one of
+// lowbias32::kDropoutRowsCandidates), or with R = 0 the R its autotuner picks
+// (written to *chosen, the candidates' mean times to ms[0..5]).
+extern "C" int device_api_dropout_rows(const float *x, float *y, uint32_t rows, uint32_t seed, float p,
+                                       uint32_t first, int R, int *chosen, float *ms)
 {
     const lowbias32::Dropout d = lowbias32::make_dropout(seed, p);
-    dropout_rows_kernel<16><<<(rows + 15u) / 16u, 256>>>(x, y, rows, d);
+    if (R == 0) {
+        R = lowbias32::dropout_rows_autotune(x, y, rows, d, first, 0, 5, ms);
+        if (R == 0) {
+            const cudaError_t e = cudaGetLastError();
+            return e != cudaSuccess ? static_cast<int>(e) : -1;
+        }
+    }
+    if (chosen) *chosen = R;
+    const cudaError_t e = lowbias32::dropout_rows(x, y, rows, d, first, R);
+    if (e != cudaSuccess) return static_cast<int>(e);
     return static_cast<int>(cudaDeviceSynchronize());
 }
 

@@ -39,7 +39,8 @@ def devlib():
         os.replace(so + ".tmp", so)
     lib = C.CDLL(so)
     lib.device_api_draws.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32] + [C.c_void_p] * 4
-    lib.device_api_dropout_rows.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32, C.c_uint32, C.c_float]
+    lib.device_api_dropout_rows.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32, C.c_uint32, C.c_float, C.c_uint32,
+                                            C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_float)]
     lib.device_api_host_hash32.argtypes = [C.c_uint32]
     lib.device_api_host_hash32.restype = C.c_uint32
     return lib
@@ -73,18 +74,57 @@ def test_header_draws_match_the_oracle_and_the_fills(devlib, orc, first):
     assert torch.equal(lib_z.view(torch.int32), z.view(torch.int32))
 
 
+CANDIDATES = (1, 2, 4, 8, 16, 32)
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("p", [0.1, 0.5])
-def test_dropout_rows_tile_kernel_equals_the_fused_fill(devlib, orc, p):
+@pytest.mark.parametrize("R", CANDIDATES)
+def test_dropout_rows_tile_kernel_equals_the_fused_fill(devlib, orc, p, R):
     import torch
 
     import dropout_lowbias32_hash32_gb300 as rng
     from dropout_lowbias32_hash32_gb300 import workloads
-    rows = 1003  # a ragged last tile of 16 rows
+    rows = 1003  # a ragged last tile for every R > 1
     x = workloads.dropout_x(rows * 256)
     xg = torch.from_numpy(x).cuda()
     y = torch.empty_like(xg)
-    assert devlib.device_api_dropout_rows(xg.data_ptr(), y.data_ptr(), rows, 42, p) == 0
+    chosen = C.c_int(-1)
+    assert devlib.device_api_dropout_rows(xg.data_ptr(), y.data_ptr(), rows, 42, p, 0, R, C.byref(chosen), None) == 0
+    assert chosen.value == R
     assert np.array_equal(y.cpu().numpy().view(np.uint32), orc.dropout(x, p, 42, 0).view(np.uint32))
     y_lib = rng.rng_dropout_fwd(xg, torch.empty_like(xg), p, 42, 0)
     assert torch.equal(y.view(torch.int32), y_lib.view(torch.int32))
+
+
+@pytest.mark.gpu
+def test_dropout_rows_autotune_picks_a_candidate_and_keeps_the_values(devlib, orc):
+    """The listing's @autotune over R: every candidate is timed on the caller's
+    buffers, the fastest is returned, and the output is the same whatever R
+    (a first counter near the 2^32 wrap)."""
+    import torch
+
+    from dropout_lowbias32_hash32_gb300 import workloads
+    rows, first = 1 << 16, U32 - 1000  # 64 MiB; counters wrap
+    x = workloads.dropout_x(rows * 256)
+    xg = torch.from_numpy(x).cuda()
+    y = torch.empty_like(xg)
+    chosen = C.c_int(-1)
+    ms = (C.c_float * len(CANDIDATES))()
+    assert devlib.device_api_dropout_rows(xg.data_ptr(), y.data_ptr(), rows, 7, 0.25, first, 0,
+                                          C.byref(chosen), ms) == 0
+    assert chosen.value in CANDIDATES
+    assert all(t > 0 for t in ms) and ms[CANDIDATES.index(chosen.value)] == min(ms)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), orc.dropout(x, 0.25, 7, first).view(np.uint32))
+
+
+@pytest.mark.gpu
+def test_dropout_rows_in_place(devlib, orc):
+    import torch
+
+    from dropout_lowbias32_hash32_gb300 import workloads
+    rows = 517
+    x = workloads.dropout_x(rows * 256)
+    yg = torch.from_numpy(x).cuda()
+    assert devlib.device_api_dropout_rows(yg.data_ptr(), yg.data_ptr(), rows, 3, 0.5, 11, 16, None, None) == 0
+    assert np.array_equal(yg.cpu().numpy().view(np.uint32), orc.dropout(x, 0.5, 3, 11).view(np.uint32))
