@@ -76,6 +76,9 @@ _SIGS = {
     "orc_fill_randn_paired": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_fill_exponential_f32": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_fill_exponential_f64": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_fill_exponential_f32_own": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_neglog_fill": (None, [_p, _sz, _p]),
+    "orc_neglog_table": (None, [_p, _p, _p, _p]),
     "orc_randn_paired": (_f64, [_u32, _u32]),
     "orc_fill_normal_f64": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_dropout_fill": (None, [_p, _f32, _u32, _u32, _sz, _p, _p]),
@@ -129,6 +132,7 @@ class Oracle:
     """numpy front end over one loaded copy of the oracle library."""
 
     def __init__(self, path: str):
+        self.path = os.path.abspath(path)  # identifies this build (each variant has its own file)
         self.lib = _bind(C.CDLL(path))
 
     # Scalar definitions ------------------------------------------------------
@@ -238,6 +242,10 @@ class Oracle:
         """binary64 values of -ln(1 - u) on the f32 uniform (not rounded to f32)."""
         return self._fill("orc_fill_exponential_f32", np.float64, seed, first, n, idx)
 
+    def fill_exponential_f32_own(self, seed, first, n=None, idx=None):
+        """binary32 values of the f32 exponential fill (the own table-driven log)."""
+        return self._fill("orc_fill_exponential_f32_own", np.float32, seed, first, n, idx)
+
     def fill_exponential_f64(self, seed, first, n=None, idx=None):
         return self._fill("orc_fill_exponential_f64", np.float64, seed, first, n, idx)
 
@@ -264,6 +272,22 @@ class Oracle:
         out = np.empty_like(t)
         self.lib.orc_zexp_fill(_ptr(t), t.size, _ptr(out))
         return out
+
+    def neglog_array(self, m):
+        """-ln(1 - m 2^-23) in binary32 by the own log, for 23-bit integers m."""
+        m = np.ascontiguousarray(m, dtype=np.uint32)
+        if m.size and int(m.max()) >= 1 << 23:
+            raise ValueError("m must be below 2^23")
+        out = np.empty(m.size, np.float32)
+        self.lib.orc_neglog_fill(_ptr(m), m.size, _ptr(out))
+        return out
+
+    def neglog_table(self):
+        """The own log's table: inv, hi, lo (257 binary32 each) and (ln2_hi, ln2_lo)."""
+        inv, hi, lo = (np.empty(257, np.float32) for _ in range(3))
+        ln2 = np.empty(2, np.float32)
+        self.lib.orc_neglog_table(_ptr(inv), _ptr(hi), _ptr(lo), _ptr(ln2))
+        return inv, hi, lo, ln2
 
     def zlog_array(self, x):
         x = np.ascontiguousarray(x, dtype=np.float64)

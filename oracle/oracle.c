@@ -36,6 +36,7 @@ typedef long double quad;
 #define Q_SQRT sqrtl
 #define Q_ERFC erfcl
 #define Q_ACOS acosl
+#define Q_RINT rintl
 #elif defined(__x86_64__)
 #include <quadmath.h>
 typedef __float128 quad;
@@ -44,6 +45,7 @@ typedef __float128 quad;
 #define Q_SQRT sqrtq
 #define Q_ERFC erfcq
 #define Q_ACOS acosq
+#define Q_RINT rintq
 #else
 #error "the oracle needs a binary128 type (aarch64 long double or x86-64 __float128)"
 #endif
@@ -345,6 +347,104 @@ double orc_exponential_f32(uint32_t seed, uint32_t counter)
     return -log(1.0 - (double)orc_uniform_f32(seed, counter));
 }
 
+/* The f32 exponential in binary32 arithmetic, this library's own logarithm
+ * (the pages' two-float neg_log_f32 is not printed; their target, every draw
+ * within 0.571 ulp, is kept).  READING: -ln(v) for v = 1 - u = V 2^-23 with
+ * the integer V = 2^23 - m in [1, 2^23] (m the uniform's 23 bits), by a
+ * table-driven reduction (Tang, "Table-driven implementation of the
+ * logarithm function in IEEE floating-point arithmetic", 1990):
+ *   V = 2^k M, M in [1, 2), E = 23 - k, so -ln v = E ln 2 - ln M;
+ *   j = round((M - 1) 256) in [0, 256], inv_j = 1/(1 + j/256) rounded to 8
+ *   significant bits, r = M inv_j - 1 (exact in binary32, |r| < 1.5 2^-8);
+ *   -ln v = (E ln 2 + ln inv_j) - log1p(r),
+ *   log1p(r) = r - r^2/2 + r^3/3 - r^4/4 + r^5/5 (Taylor; the next term is
+ *   below 2^-37 of the result).
+ * E ln 2 + ln inv_j is carried as hi + lo: ln 2 and ln inv_j are split into
+ * a multiple of 2^-19 (hi) and the binary32 rounding of the rest (lo), so
+ * E ln2_hi + hi_j is exact; hi - r is summed exactly (TwoSum, Knuth TAOCP
+ * vol. 2, 4.2.2), its error, the lo terms and the Taylor tail added after,
+ * and the result rounded once at the end.  Every operation below is one
+ * IEEE binary32 operation (fmaf a single rounding). */
+static float neglog_inv[257], neglog_hi[257], neglog_lo[257];
+static float neglog_ln2_hi, neglog_ln2_lo;
+static int neglog_ready;
+
+/* x > 0 rounded to p significant bits, to nearest (ties to even) */
+static double round_to_bits(double x, int p)
+{
+    int e;
+    double m = frexp(x, &e); /* x = m 2^e, m in [0.5, 1) */
+    return ldexp(nearbyint(ldexp(m, p)), e - p);
+}
+
+static void neglog_split(quad v, float *hi, float *lo)
+{
+    quad h = Q_RINT(v * 524288) / 524288; /* nearest multiple of 2^-19 */
+    *hi = (float)h;                        /* exact: at most 20 bits */
+    *lo = (float)(v - h);                  /* one rounding */
+}
+
+static void neglog_init(void)
+{
+    if (neglog_ready) return;
+    for (int j = 0; j <= 256; ++j) {
+        /* 1/(1 + j/256) = 256/(256 + j); binary64 then 8 bits rounds as the
+         * exact value would: no 256/(256 + j) lies on an 8-bit midpoint */
+        neglog_inv[j] = (float)round_to_bits(256.0 / (256.0 + j), 8);
+        neglog_split(Q_LOG((quad)neglog_inv[j]), &neglog_hi[j], &neglog_lo[j]);
+    }
+    neglog_split(Q_LOG((quad)2), &neglog_ln2_hi, &neglog_ln2_lo);
+    neglog_ready = 1;
+}
+
+void orc_neglog_table(float *inv, float *hi, float *lo, float *ln2)
+{
+    neglog_init();
+    for (int j = 0; j <= 256; ++j) {
+        inv[j] = neglog_inv[j];
+        hi[j] = neglog_hi[j];
+        lo[j] = neglog_lo[j];
+    }
+    ln2[0] = neglog_ln2_hi;
+    ln2[1] = neglog_ln2_lo;
+}
+
+/* -ln(1 - m 2^-23) in binary32, m in [0, 2^23) */
+float orc_neglog_f32(uint32_t m)
+{
+    neglog_init();
+    uint32_t V = 8388608u - m;
+    float x = (float)V; /* exact: V <= 2^23 */
+    uint32_t bits;
+    memcpy(&bits, &x, sizeof bits);
+    int k = (int)(bits >> 23) - 127;
+    uint32_t mant = bits & 8388607u;
+    uint32_t mbits = mant | 0x3F800000u;
+    float M;
+    memcpy(&M, &mbits, sizeof M);
+    uint32_t j = (mant + 16384u) >> 15; /* round((M - 1) 256) */
+    float E = (float)(23 - k);
+    float r = fmaf(M, neglog_inv[j], -1.0f);
+    float t_hi = fmaf(E, neglog_ln2_hi, neglog_hi[j]);
+    float t_lo = fmaf(E, neglog_ln2_lo, neglog_lo[j]);
+    float s = t_hi - r;
+    float bb = s - t_hi;
+    float err = (t_hi - (s - bb)) + (-r - bb);
+    float r2 = r * r;
+    float p = fmaf(r, -0x1.99999ap-3f, 0.25f); /* 1/4 - r/5 */
+    p = fmaf(r, p, -0x1.555556p-2f);           /* -1/3 + r/4 - r^2/5 */
+    p = fmaf(r, p, 0.5f);                      /* 1/2 - r/3 + r^2/4 - r^3/5 */
+    float tail = r2 * p;                       /* -log1p(r) - (-r) */
+    float c = (err + t_lo) + tail;
+    return s + c;
+}
+
+/* The f32 exponential fill's value: -ln(1 - u) through orc_neglog_f32. */
+float orc_exponential_f32_own(uint32_t seed, uint32_t counter)
+{
+    return orc_neglog_f32(orc_draw32(seed, counter) & 8388607u);
+}
+
 double orc_exponential_f64(uint32_t seed, uint32_t counter)
 {
     double v = 1.0 - orc_uniform_f64(seed, counter);
@@ -599,6 +699,16 @@ void orc_fill_randn_paired(uint32_t seed, uint32_t first, size_t n, const uint64
 void orc_fill_exponential_f32(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)
 {
     for (size_t i = 0; i < n; ++i) out[i] = orc_exponential_f32(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_exponential_f32_own(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, float *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_exponential_f32_own(seed, counter_of(first, idx, i));
+}
+
+void orc_neglog_fill(const uint32_t *m, size_t n, float *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_neglog_f32(m[i]);
 }
 
 void orc_fill_exponential_f64(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)

@@ -215,7 +215,7 @@ _LOW23_CACHE = {}
 
 def _counters_with_low23(orc, seed: int, word: int, targets, first_n: int = 1 << 26):
     """Counters c (< first_n / 2) whose uniform at 2c + word has the given 23-bit grid index."""
-    key = (id(orc), seed, word, first_n)
+    key = (orc.path, seed, word, first_n)
     if key not in _LOW23_CACHE:
         _LOW23_CACHE.clear()
         _LOW23_CACHE[key] = orc.fill_u32(seed, word, first_n)[::2] & 0x7FFFFF
@@ -325,6 +325,95 @@ def pin_exponentials(orc):
     for x in (e, e64):
         assert abs(x.mean() - 1) < 5 / math.sqrt(n) and abs(x.var() - 1) < 5 * math.sqrt(8 / n)
         assert stats.chisquare(np.histogram(x, bins=edges)[0]).pvalue > 1e-3
+
+
+_NEGLOG_CACHE = {}
+
+
+def _neglog_all(orc):
+    """The own f32 log on every 23-bit input, with the binary64 -ln(1 - u)
+    (numpy's log of the exact binary64 value 1 - u: within 2^-52 relative)."""
+    if orc.path not in _NEGLOG_CACHE:
+        _NEGLOG_CACHE.clear()
+        m = np.arange(1 << 23, dtype=np.uint32)
+        ref = -np.log((8388608.0 - m) * 2.0 ** -23)
+        _NEGLOG_CACHE[orc.path] = (m, orc.neglog_array(m), ref)
+    return _NEGLOG_CACHE[orc.path]
+
+
+def pin_neglog_f32_exhaustive(orc):
+    """The f32 exponential's own log against the exact -ln(1 - u) on all 2^23
+    inputs (tandem-cuda "Performance" and tandem-sycl "Design", Exponentials:
+    every draw within 0.571 ulp).  Measured: within 0.5027 ulp (0.5044 without
+    the r^5 Taylor term), and the correctly rounded binary32 value on all but
+    98 inputs, where the exact value lies within 0.003 ulp of a rounding
+    boundary; u = 0 gives +0 and the top of the grid 23 ln 2 rounded."""
+    m, e, ref = _neglog_all(orc)
+    nz = ref > 0
+    ulp = np.spacing(ref[nz].astype(np.float32)).astype(np.float64)
+    err = np.abs(e[nz].astype(np.float64) - ref[nz]) / ulp
+    assert err.max() <= 0.5035
+    assert np.count_nonzero(e != ref.astype(np.float32)) <= 120
+    assert e[0] == 0 and not np.signbit(e[0])
+    assert e[-1] == np.float32(23 * math.log(2))
+    assert np.all(np.diff(e) >= 0)  # monotone in u
+
+
+def pin_neglog_f32_maps_back(orc):
+    """1 - exp(-e) maps every value back to its own draw's grid point (the
+    property the pages' 0.571 ulp bound is for): round(2^23 (1 - exp(-e))) = m."""
+    m, e, _ = _neglog_all(orc)
+    back = np.rint(-np.expm1(-e.astype(np.float64)) * 8388608.0)
+    assert np.array_equal(back.astype(np.int64), m.astype(np.int64))
+
+
+def pin_neglog_f32_table(orc):
+    """The own log's table against its definition: inv_j is 256/(256 + j)
+    rounded to 8 significant bits (exact rationals), hi_j the nearest multiple
+    of 2^-19 to ln inv_j and hi_j + lo_j = ln inv_j within 2^-43; ln2_hi and
+    ln2_lo likewise for ln 2;
+    and for every 24-bit M in [1, 2) with its bin j, M inv_j - 1 is exact in
+    binary32 (the reduction step rounds nothing)."""
+    from fractions import Fraction
+    inv, hi, lo, ln2 = orc.neglog_table()
+    for j in range(257):
+        x = Fraction(256, 256 + j)
+        e = x.numerator.bit_length() - x.denominator.bit_length()  # 2^e <= x < 2^(e+1) or 2^(e-1) <= ...
+        if Fraction(2) ** e > x:
+            e -= 1
+        scaled = x / Fraction(2) ** (e - 7)  # in [128, 256)
+        q, rem = divmod(scaled.numerator, scaled.denominator)
+        if 2 * rem > scaled.denominator or (2 * rem == scaled.denominator and q % 2):
+            q += 1
+        assert Fraction(float(inv[j])) == q * Fraction(2) ** (e - 7), j
+        for h, l, v in ((hi[j], lo[j], math.log(float(inv[j]))), (ln2[0], ln2[1], math.log(2))):
+            scaled = v * 2 ** 19  # binary64 is enough: no value lies near a tie
+            assert abs(scaled - math.floor(scaled) - 0.5) > 1e-6
+            assert float(h) == round(scaled) / 2 ** 19  # the nearest multiple of 2^-19
+            assert abs(float(h) + float(l) - v) <= 2.0 ** -43
+    mant = np.arange(1 << 23, dtype=np.int64)
+    j = (mant + 16384) >> 15
+    num = (8388608 + mant) * (inv.astype(np.float64)[j] * 512).astype(np.int64) - (1 << 32)  # r 2^32
+    odd = num.copy()
+    nzr = odd != 0
+    while True:
+        even = nzr & (odd % 2 == 0)
+        if not even.any():
+            break
+        odd[even] //= 2
+    assert np.all(np.abs(odd) < (1 << 24))
+    assert np.abs(num).max() < 1.5 * 2.0 ** -8 * 2 ** 32
+
+
+def pin_exponential_f32_fill(orc):
+    """The f32 exponential fill is the own log of the draw's 23 bits, within
+    0.505 ulp of -log(1 - u) in binary64 on the same counters."""
+    n = 1 << 20
+    e = orc.fill_exponential_f32_own(13, 7, n).astype(np.float64)
+    ref = orc.fill_exponential_f32(13, 7, n)
+    nz = ref > 0
+    assert np.all(e[~nz] == 0)
+    assert (np.abs(e[nz] - ref[nz]) / np.spacing(ref[nz].astype(np.float32))).max() <= 0.505
 
 
 # ---------------------------------------------------------------- dropout --
@@ -486,6 +575,7 @@ def pin_slice_invariant(orc):
         lambda f, m, idx=None: orc.fill_f16_bits(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_randn_paired(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_exponential_f32(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_exponential_f32_own(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_exponential_f64(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_u32(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_u64(9, f, m, idx),
@@ -514,7 +604,9 @@ ALL_PINS = [
     pin_tile_mean, pin_uniform_grid, pin_hash_bijective, pin_draw64_words, pin_narrow_fills,
     pin_lemire_exhaustive_8bit, pin_lemire_exhaustive_16bit, pin_lemire_wide_words,
     pin_below_distributions, pin_ranges_wrap, pin_randn_special_angles,
-    pin_randn_tail_end, pin_randn_distribution, pin_randn_paired, pin_exponentials, pin_dropout, pin_zexp_zlog,
+    pin_randn_tail_end, pin_randn_distribution, pin_randn_paired, pin_exponentials,
+    pin_neglog_f32_exhaustive, pin_neglog_f32_maps_back, pin_neglog_f32_table, pin_exponential_f32_fill,
+    pin_dropout, pin_zexp_zlog,
     pin_zig_table_published, pin_zig_table_invariants, pin_zig_miss_rate,
     pin_normal_f64_distribution, pin_zig_wedge_acceptance, pin_slice_invariant,
 ]
