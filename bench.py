@@ -125,14 +125,16 @@ def next_specs():
 
 
 def selected_specs(only: str | None):
+    """The step's fills, or with --only the named fills of the step or beyond it."""
     specs = fill_specs()
     if not only:
         return specs
+    every = specs + next_specs()
     want = only.split(",")
-    unknown = set(want) - {s.name for s in specs}
+    unknown = set(want) - {s.name for s in every}
     if unknown:
         raise SystemExit(f"unknown fills: {sorted(unknown)}")
-    return [s for s in specs if s.name in want]
+    return [s for s in every if s.name in want]
 
 
 # ------------------------------------------------------------------ peaks --
@@ -269,6 +271,13 @@ def oracle_calls(orc, n_sample: int):
         "dropout_bwd_p0.1": drop(dy, 0.1),
         "dropout_fwd_p0.5": drop(x, 0.5),
         "dropout_bwd_p0.5": drop(dy, 0.5),
+        "normal_f32_pairs": lambda first, off, n: orc.fill_randn_paired(W.NORMAL_SEED, first + off, n),
+        "exponential_f32": lambda first, off, n: orc.fill_exponential_f32_own(W.NORMAL_SEED, first + off, n),
+        "exponential_f64": lambda first, off, n: orc.fill_exponential_f64(W.NORMAL_SEED, first + off, n),
+        "u8": lambda first, off, n: orc.fill_u8(W.UNIFORM_SEED, first + off, n),
+        "u16": lambda first, off, n: orc.fill_u16(W.UNIFORM_SEED, first + off, n),
+        "f16": lambda first, off, n: orc.fill_f16_bits(W.UNIFORM_SEED, first + off, n),
+        "bool": lambda first, off, n: orc.fill_bool(W.UNIFORM_SEED, first + off, n),
     }
 
 
@@ -363,7 +372,9 @@ def run_ours(args):
     dy = host_dy.to(dev) if needs_inputs else None
     y = torch.empty(n, dtype=torch.float32, device=dev) if needs_inputs else None
     outs = {"int32": buf4, "float32": buf4.view(torch.float32), "int64": buf8,
-            "float64": buf8.view(torch.float64), "x": (x, y), "dy": (dy, y)}
+            "float64": buf8.view(torch.float64), "x": (x, y), "dy": (dy, y),
+            "uint8": buf4.view(torch.uint8)[:n], "int16": buf4.view(torch.int16)[:n],
+            "float16": buf4.view(torch.float16)[:n], "bool": buf4.view(torch.bool)[:n]}
     stream = torch.cuda.current_stream(dev)
     # rank r fills elements [r n, (r + 1) n) of each global fill
     base = (rank * n) & 0xFFFFFFFF

@@ -2,11 +2,13 @@
 //
 // tandem-sycl "Design", section Exponentials, and tandem-cuda
 // "Performance", rows fill_exponential_f64 / _f32: exponentials by a
-// logarithm of a uniform, f64 through the library's own logarithm (bit for
-// bit reproducible) and f32 within a stated accuracy.  Restated on hash32:
-//   f32: e = -ln(1 - u), u = uniform(seed, c) on the 2^-23 grid; 1 - u is
-//        exact, ln is CUDA's logf (within 1 ulp), so e is within 2 ulp of
-//        the exact value; e in [0, 23 ln 2].
+// logarithm of a uniform, f64 through the library's own logarithm and f32
+// through an own binary32 logarithm within 0.571 ulp, both reproducible bit
+// for bit.  Restated on hash32:
+//   f32: e = -ln(1 - u), u = uniform(seed, c) on the 2^-23 grid, by
+//        lowbias32::neg_log_grid of include/rng_device.cuh (a table-driven
+//        binary32 logarithm, within 0.5035 ulp of the exact value on every
+//        input); e in [0, 23 ln 2].
 //   f64: e = 0 - zlog(1 - u), u = (D64 >> 11) 2^-53; 1 - u is exact and
 //        zlog is the fixed IEEE sequence of f64_math.cuh, so the value is
 //        reproducible bit for bit; e in [0, 53 ln 2].

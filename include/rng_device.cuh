@@ -9,7 +9,8 @@
 //   uniform      = (draw32 & 0x7FFFFF) * 2^-23         (section uniform);
 //   randn        = sqrt(-2 ln(1 - u(2c))) cos(2 pi u(2c + 1))  (section randn);
 //   dropout      = uniform >= p ? x / (1 - p) : 0       (section dropout);
-//   exponential  = -ln(1 - uniform)  (tandem-sycl "Design", section Exponentials).
+//   exponential  = -ln(1 - uniform), the own f32 logarithm neg_log_grid
+//                  (tandem-sycl "Design", section Exponentials).
 // A kernel that gives element e the counter first + e draws exactly what
 // the corresponding fill writes: dropout() is bit-identical to
 // rng_dropout_fwd, uniform() to rng_fill_f32, draw32() to rng_fill_u32;
@@ -18,8 +19,9 @@
 // one seed disjoint counters (randn reads the uniforms at 2c and 2c + 1).
 //
 // Keys are made once on the host (make_key, make_dropout) and passed to the
-// kernel by value.  The header needs only <stdint.h> and nvcc.  It also holds
-// the page's dropout_rows tile kernel with its R autotuner.
+// kernel by value.  The header needs only <stdint.h>, nvcc and the generated
+// table beside it (lowbias32_neglog_table.inc).  It also holds the page's
+// dropout_rows tile kernel with its R autotuner.
 #pragma once
 
 #include <stdint.h>
@@ -173,14 +175,54 @@ __device__ __forceinline__ float randn_paired(Key k, uint32_t c)
 
 // ---- exponential ----------------------------------------------------------------
 
-// -ln(1 - u) for u = uniform(k, c): 1 - u = 2 - (1 + u) exactly, CUDA's logf
-// (within 1 ulp), so the value is within 2 ulp of the exact one; 0 - ln
-// keeps u = 0 at +0.
-__device__ __forceinline__ float exponential(Key k, uint32_t c)
+namespace detail {
+#include "lowbias32_neglog_table.inc"
+}  // namespace detail
+
+// -ln(1 - m 2^-23) for a 23-bit m, in binary32 arithmetic: the library's own
+// logarithm (tandem-sycl "Design", Exponentials: an own f32 logarithm, every
+// draw within 0.571 ulp).  1 - m 2^-23 = V 2^-23 with the integer V = 2^23 - m;
+// V = 2^k M, M in [1, 2), E = 23 - k; the bin j = round((M - 1) 256) gives
+// inv_j (8 bits) and ln inv_j = hi_j + lo_j from a 4 KiB table, so
+//   -ln(1 - u) = (E ln 2 + ln inv_j) - log1p(r),  r = M inv_j - 1 (exact),
+// with E ln2_hi + hi_j exact, hi - r summed exactly (TwoSum), the error,
+// the lo parts and the Taylor tail r^2/2 - r^3/3 + r^4/4 - r^5/5 added after
+// and one rounding at the end.  Within 0.5035 ulp of the exact value on all
+// 2^23 inputs (correctly rounded on all but 98); m = 0 gives +0.  Every step
+// is an explicit IEEE operation, so the result is the same bits on any
+// IEEE machine that performs the same sequence.
+namespace detail {
+// The integer x in [0, 2^23] as binary32, exactly: 2^23 + x has x in its
+// significand (x = 2^23 carries into the exponent: 2^24), and subtracting
+// 2^23 is exact.  An ALU and an FMA-pipe operation instead of a conversion.
+__device__ __forceinline__ float small_uint_to_float(uint32_t x)
 {
-    const float one_minus_u = 2.0f - __uint_as_float(0x3F800000u | (draw32(k, c) & 0x7FFFFFu));
-    return 0.0f - logf(one_minus_u);
+    return __fsub_rn(__uint_as_float(0x4B000000u | x), 8388608.0f);
 }
+}  // namespace detail
+
+__device__ __forceinline__ float neg_log_grid(uint32_t m)
+{
+    const uint32_t bits = __float_as_uint(detail::small_uint_to_float(0x800000u - m));  // V, exact
+    const uint32_t mant = bits & 0x7FFFFFu;
+    const float M = __uint_as_float(mant | 0x3F800000u);
+    const float4 t = __ldg(&detail::kNegLogTable[(mant + 16384u) >> 15]);  // {inv_j, hi_j, lo_j, 0}
+    const float E = detail::small_uint_to_float(150u - (bits >> 23));      // 23 - k
+    const float r = __fmaf_rn(M, t.x, -1.0f);
+    const float t_hi = __fmaf_rn(E, detail::kNegLogLn2Hi, t.y);
+    const float t_lo = __fmaf_rn(E, detail::kNegLogLn2Lo, t.z);
+    const float s = __fsub_rn(t_hi, r);
+    const float bb = __fsub_rn(s, t_hi);
+    const float err = __fadd_rn(__fsub_rn(t_hi, __fsub_rn(s, bb)), __fsub_rn(-r, bb));
+    float p = __fmaf_rn(r, -0x1.99999ap-3f, 0.25f);  // 1/4 - r/5
+    p = __fmaf_rn(r, p, -0x1.555556p-2f);           // -1/3 + r/4 - r^2/5
+    p = __fmaf_rn(r, p, 0.5f);                      // 1/2 - r/3 + r^2/4 - r^3/5
+    const float tail = __fmul_rn(__fmul_rn(r, r), p);
+    return __fadd_rn(s, __fadd_rn(__fadd_rn(err, t_lo), tail));
+}
+
+// -ln(1 - u) for u = uniform(k, c), by neg_log_grid; in [0, 23 ln 2].
+__device__ __forceinline__ float exponential(Key k, uint32_t c) { return neg_log_grid(draw32(k, c) & 0x7FFFFFu); }
 
 // ---- dropout ------------------------------------------------------------------
 

@@ -7,7 +7,7 @@
 namespace {
 
 __global__ void draw_kernel(uint32_t seed, uint32_t first, uint32_t n, uint32_t *d32, uint64_t *d64, float *u,
-                            float *z)
+                            float *z, float *ex)
 {
     const lowbias32::Key k = lowbias32::make_key(seed);
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
@@ -16,15 +16,16 @@ __global__ void draw_kernel(uint32_t seed, uint32_t first, uint32_t n, uint32_t 
         d64[i] = lowbias32::draw64(k, c);
         u[i] = lowbias32::uniform(k, c);
         z[i] = lowbias32::randn(k, c);
+        ex[i] = lowbias32::exponential(k, c);
     }
 }
 
 }  // namespace
 
 extern "C" int device_api_draws(uint32_t seed, uint32_t first, uint32_t n, uint32_t *d32, uint64_t *d64, float *u,
-                                float *z)
+                                float *z, float *ex)
 {
-    draw_kernel<<<256, 256>>>(seed, first, n, d32, d64, u, z);
+    draw_kernel<<<256, 256>>>(seed, first, n, d32, d64, u, z, ex);
     return static_cast<int>(cudaDeviceSynchronize());
 }
 
@@ -45,6 +46,20 @@ extern "C" int device_api_dropout_rows(const float *x, float *y, uint32_t rows, 
     if (chosen) *chosen = R;
     const cudaError_t e = lowbias32::dropout_rows(x, y, rows, d, first, R);
     if (e != cudaSuccess) return static_cast<int>(e);
+    return static_cast<int>(cudaDeviceSynchronize());
+}
+
+// The header's own f32 logarithm on given 23-bit inputs: out[i] =
+// -ln(1 - m[i] 2^-23) by lowbias32::neg_log_grid.
+__global__ void neglog_kernel(const uint32_t *m, float *out, uint32_t n)
+{
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        out[i] = lowbias32::neg_log_grid(m[i] & 0x7FFFFFu);
+}
+
+extern "C" int device_api_neglog(const uint32_t *m, float *out, uint32_t n)
+{
+    neglog_kernel<<<1024, 256>>>(m, out, n);
     return static_cast<int>(cudaDeviceSynchronize());
 }
 

@@ -19,7 +19,7 @@ U32 = 1 << 32
 
 
 @pytest.mark.parametrize("name", ["u32", "u64_below_1000", "i64_range", "normal_f32", "normal_f64",
-                                  "dropout_fwd_p0.5"])
+                                  "dropout_fwd_p0.5", "exponential_f32", "u8", "normal_f32_pairs"])
 @pytest.mark.parametrize("first", [0, U32 - 1000])
 def test_split_equals_one_call(orc, name, first):
     n = 4099  # ranges of unequal length; the second case wraps the counter
@@ -31,8 +31,14 @@ def test_split_equals_one_call(orc, name, first):
             assert split.dtype == whole.dtype and split.tobytes() == whole.tobytes()
 
 
-def test_oracle_calls_cover_the_step(orc):
-    assert set(bench.oracle_calls(orc, 16)) == {s.name for s in bench.fill_specs()}
+def test_oracle_calls_cover_every_fill(orc):
+    assert set(bench.oracle_calls(orc, 16)) == {s.name for s in bench.fill_specs() + bench.next_specs()}
+
+
+def test_only_selects_fills_of_the_step_and_beyond():
+    assert [s.name for s in bench.selected_specs("u32,exponential_f32")] == ["u32", "exponential_f32"]
+    with pytest.raises(SystemExit):
+        bench.selected_specs("no_such_fill")
 
 
 def test_reference_arm_prints_the_contract_line():

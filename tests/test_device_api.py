@@ -31,19 +31,52 @@ def devlib():
         pytest.skip("nvcc not available")
     os.makedirs(BUILD, exist_ok=True)
     so = os.path.join(BUILD, "libdevice_api_kernels.so")
-    if not os.path.exists(so) or os.path.getmtime(so) < max(
-            os.path.getmtime(SRC), os.path.getmtime(os.path.join(ROOT, "include", "rng_device.cuh"))):
+    deps = [SRC] + [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))]
+    if not os.path.exists(so) or os.path.getmtime(so) < max(os.path.getmtime(d) for d in deps):
         subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
                         "-I" + os.path.join(ROOT, "include"), "-Xcompiler", "-fPIC", "-shared", SRC,
                         "-o", so + ".tmp"], check=True)
         os.replace(so + ".tmp", so)
     lib = C.CDLL(so)
-    lib.device_api_draws.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32] + [C.c_void_p] * 4
+    lib.device_api_draws.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32] + [C.c_void_p] * 5
+    lib.device_api_neglog.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32]
     lib.device_api_dropout_rows.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32, C.c_uint32, C.c_float, C.c_uint32,
                                             C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_float)]
     lib.device_api_host_hash32.argtypes = [C.c_uint32]
     lib.device_api_host_hash32.restype = C.c_uint32
     return lib
+
+
+def test_header_neglog_table_matches_the_oracle(orc):
+    """The header's generated table (gen_neglog_table.py: exact rationals and
+    mpmath) equals the oracle's own (binary64 and binary128 in C), entry by
+    entry: two derivations from the same definition."""
+    import re
+    txt = open(os.path.join(ROOT, "include", "lowbias32_neglog_table.inc")).read()
+
+    def val(t):
+        t = t.strip()
+        assert t.endswith("f"), t
+        return float.fromhex(t[:-1]) if "x" in t else float(t[:-1])
+
+    rows = re.findall(r"^    \{([^}]*)\},", txt, re.M)
+    table = np.array([[val(x) for x in r.split(",")] for r in rows])
+    inv, hi, lo, ln2 = orc.neglog_table()
+    assert table.shape == (257, 4)
+    assert np.array_equal(table[:, 0], inv) and np.array_equal(table[:, 1], hi) and np.array_equal(table[:, 2], lo)
+    consts = dict(re.findall(r"kNegLogLn2(Hi|Lo) = ([^;]+);", txt))
+    assert val(consts["Hi"]) == ln2[0] and val(consts["Lo"]) == ln2[1]
+
+
+@pytest.mark.gpu
+def test_header_neglog_on_every_input(devlib, orc):
+    """neg_log_grid on all 2^23 inputs equals the oracle's own f32 log, bit for bit."""
+    import torch
+    m = np.arange(1 << 23, dtype=np.uint32)
+    mg = torch.from_numpy(m.view(np.int32)).cuda()
+    out = torch.empty(m.size, dtype=torch.float32, device="cuda")
+    assert devlib.device_api_neglog(mg.data_ptr(), out.data_ptr(), m.size) == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), orc.neglog_array(m).view(np.uint32))
 
 
 def test_header_hash_on_the_host_matches_the_oracle(devlib, orc):
@@ -62,7 +95,9 @@ def test_header_draws_match_the_oracle_and_the_fills(devlib, orc, first):
     d64 = torch.empty(n, dtype=torch.int64, device="cuda")
     u = torch.empty(n, dtype=torch.float32, device="cuda")
     z = torch.empty(n, dtype=torch.float32, device="cuda")
-    assert devlib.device_api_draws(seed, first, n, d32.data_ptr(), d64.data_ptr(), u.data_ptr(), z.data_ptr()) == 0
+    ex = torch.empty(n, dtype=torch.float32, device="cuda")
+    assert devlib.device_api_draws(seed, first, n, d32.data_ptr(), d64.data_ptr(), u.data_ptr(), z.data_ptr(),
+                                   ex.data_ptr()) == 0
     assert np.array_equal(d32.cpu().numpy().view(np.uint32), orc.fill_u32(seed, first, n))
     assert np.array_equal(d64.cpu().numpy().view(np.uint64), orc.fill_u64(seed, first, n))
     assert np.array_equal(u.cpu().numpy().view(np.uint32), orc.fill_f32(seed, first, n).view(np.uint32))
@@ -72,6 +107,10 @@ def test_header_draws_match_the_oracle_and_the_fills(devlib, orc, first):
     # the fused draw is the library fill's element, bit for bit
     lib_z = rng.rng_fill_normal_f32(seed, first, torch.empty(n, dtype=torch.float32, device="cuda"))
     assert torch.equal(lib_z.view(torch.int32), z.view(torch.int32))
+    assert np.array_equal(ex.cpu().numpy().view(np.uint32),
+                          orc.fill_exponential_f32_own(seed, first, n).view(np.uint32))
+    lib_ex = rng.rng_fill_exponential_f32(seed, first, torch.empty(n, dtype=torch.float32, device="cuda"))
+    assert torch.equal(lib_ex.view(torch.int32), ex.view(torch.int32))
 
 
 CANDIDATES = (1, 2, 4, 8, 16, 32)
