@@ -78,6 +78,9 @@ _SIGS = {
     "orc_fill_exponential_f64": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_fill_exponential_f32_own": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_neglog_fill": (None, [_p, _sz, _p]),
+    "orc_fill_randn_precise": (None, [_u32, _u32, _sz, _p, _p]),
+    "orc_cos2pi_fill": (None, [_p, _sz, _p]),
+    "orc_cos2pi_coefficients": (None, [_p]),
     "orc_neglog_table": (None, [_p, _p, _p, _p]),
     "orc_randn_paired": (_f64, [_u32, _u32]),
     "orc_fill_normal_f64": (None, [_u32, _u32, _sz, _p, _p]),
@@ -242,6 +245,10 @@ class Oracle:
         """binary64 values of -ln(1 - u) on the f32 uniform (not rounded to f32)."""
         return self._fill("orc_fill_exponential_f32", np.float64, seed, first, n, idx)
 
+    def fill_randn_precise(self, seed, first, n=None, idx=None):
+        """binary32 values of the precise f32 normal fill (randn's definition to a few ulp)."""
+        return self._fill("orc_fill_randn_precise", np.float32, seed, first, n, idx)
+
     def fill_exponential_f32_own(self, seed, first, n=None, idx=None):
         """binary32 values of the f32 exponential fill (the own table-driven log)."""
         return self._fill("orc_fill_exponential_f32_own", np.float32, seed, first, n, idx)
@@ -280,6 +287,21 @@ class Oracle:
             raise ValueError("m must be below 2^23")
         out = np.empty(m.size, np.float32)
         self.lib.orc_neglog_fill(_ptr(m), m.size, _ptr(out))
+        return out
+
+    def cos2pi_array(self, m):
+        """cos(2 pi m 2^-23) in binary32 by the own routine, for 23-bit integers m."""
+        m = np.ascontiguousarray(m, dtype=np.uint32)
+        if m.size and int(m.max()) >= 1 << 23:
+            raise ValueError("m must be below 2^23")
+        out = np.empty(m.size, np.float32)
+        self.lib.orc_cos2pi_fill(_ptr(m), m.size, _ptr(out))
+        return out
+
+    def cos2pi_coefficients(self):
+        """s1_hi s1_lo s3 s5 s7 s9 c2_hi c2_lo c4 c6 c8 c10 (binary32)."""
+        out = np.empty(12, np.float32)
+        self.lib.orc_cos2pi_coefficients(_ptr(out))
         return out
 
     def neglog_table(self):

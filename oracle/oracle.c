@@ -439,6 +439,88 @@ float orc_neglog_f32(uint32_t m)
     return s + c;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Precise f32 normal [Tandem-D, section Normals: the default float normal   */
+/* agrees with other ports to 16 ulp + 1e-6; a precise f32 Box-Muller is a   */
+/* build option].  READING: an opt-in fill with randn's definition (the      */
+/* uniforms at 2c and 2c + 1, cosine branch) evaluated in binary32 to a few  */
+/* ulp: z = sqrt(2 NL(u0)) cos(2 pi u1), NL the own -ln(1 - u) above, an     */
+/* IEEE square root, and the own cos(2 pi u1) below.                          */
+/* ------------------------------------------------------------------------ */
+
+/* cos(2 pi m 2^-23): the quadrant q = m >> 21 and g = (m mod 2^21) 2^-23 in
+ * [0, 1/4) are exact; cos(2 pi (q/4 + g)) is cos g, -sin g, -cos g or sin g
+ * (in turns of 2 pi); above g = 1/8 the complement h = 1/4 - g (exact)
+ * swaps sin and cos.  On x = k 2^-23 <= 1/8 the Taylor series of sin(2 pi x)
+ * to x^9 and cos(2 pi x) to x^10 (truncation below 2^-28 relative), each
+ * coefficient (2 pi)^n / n! rounded once to binary32, the leading ones (2 pi
+ * and -(2 pi)^2/2) as hi + lo so that their rounding does not reach the
+ * result. */
+static float cp_s1_hi, cp_s1_lo, cp_s3, cp_s5, cp_s7, cp_s9;
+static float cp_c2_hi, cp_c2_lo, cp_c4, cp_c6, cp_c8, cp_c10;
+static int cp_ready;
+
+static void cos2pi_init(void)
+{
+    if (cp_ready) return;
+    quad tp = 2 * Q_ACOS((quad)-1); /* 2 pi */
+    quad term[11];                   /* term[n] = (2 pi)^n / n! */
+    term[0] = 1;
+    for (int n = 1; n <= 10; ++n) term[n] = term[n - 1] * tp / n;
+    cp_s1_hi = (float)term[1];
+    cp_s1_lo = (float)(term[1] - cp_s1_hi);
+    cp_s3 = (float)(-term[3]);
+    cp_s5 = (float)term[5];
+    cp_s7 = (float)(-term[7]);
+    cp_s9 = (float)term[9];
+    cp_c2_hi = (float)(-term[2]);
+    cp_c2_lo = (float)(-term[2] - cp_c2_hi);
+    cp_c4 = (float)term[4];
+    cp_c6 = (float)(-term[6]);
+    cp_c8 = (float)term[8];
+    cp_c10 = (float)(-term[10]);
+    cp_ready = 1;
+}
+
+void orc_cos2pi_coefficients(float *out) /* s1_hi s1_lo s3 s5 s7 s9 c2_hi c2_lo c4 c6 c8 c10 */
+{
+    cos2pi_init();
+    const float v[12] = {cp_s1_hi, cp_s1_lo, cp_s3, cp_s5, cp_s7, cp_s9,
+                         cp_c2_hi, cp_c2_lo, cp_c4, cp_c6, cp_c8, cp_c10};
+    for (int i = 0; i < 12; ++i) out[i] = v[i];
+}
+
+float orc_cos2pi_grid(uint32_t m)
+{
+    cos2pi_init();
+    uint32_t q = m >> 21;
+    uint32_t f = m & 0x1FFFFFu;
+    int swap = f > 0x100000u;
+    uint32_t k = swap ? 0x200000u - f : f;
+    float x = (float)k * 0x1p-23f; /* exact: k <= 2^20 */
+    float x2 = x * x;
+    float p = fmaf(x2, cp_s9, cp_s7);
+    p = fmaf(x2, p, cp_s5);
+    p = fmaf(x2, p, cp_s3);
+    p = fmaf(x2, p, cp_s1_lo);
+    float sin_x = fmaf(x, cp_s1_hi, x * p);
+    float c = fmaf(x2, cp_c10, cp_c8);
+    c = fmaf(x2, c, cp_c6);
+    c = fmaf(x2, c, cp_c4);
+    float t = x2 * fmaf(x2, c, cp_c2_lo);
+    float cos_x = 1.0f + fmaf(x2, cp_c2_hi, t);
+    float v = ((int)(q & 1u) ^ swap) ? sin_x : cos_x;
+    return (q == 1u || q == 2u) ? -v : v;
+}
+
+/* randn(seed, counter) in binary32 to a few ulp */
+float orc_randn_precise(uint32_t seed, uint32_t counter)
+{
+    float e = orc_neglog_f32(orc_draw32(seed, 2u * counter) & 8388607u);
+    float r = sqrtf(e + e); /* 2 e exact; IEEE square root */
+    return r * orc_cos2pi_grid(orc_draw32(seed, 2u * counter + 1u) & 8388607u);
+}
+
 /* The f32 exponential fill's value: -ln(1 - u) through orc_neglog_f32. */
 float orc_exponential_f32_own(uint32_t seed, uint32_t counter)
 {
@@ -704,6 +786,16 @@ void orc_fill_exponential_f32(uint32_t seed, uint32_t first, size_t n, const uin
 void orc_fill_exponential_f32_own(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, float *out)
 {
     for (size_t i = 0; i < n; ++i) out[i] = orc_exponential_f32_own(seed, counter_of(first, idx, i));
+}
+
+void orc_fill_randn_precise(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, float *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_randn_precise(seed, counter_of(first, idx, i));
+}
+
+void orc_cos2pi_fill(const uint32_t *m, size_t n, float *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_cos2pi_grid(m[i]);
 }
 
 void orc_neglog_fill(const uint32_t *m, size_t n, float *out)

@@ -416,6 +416,63 @@ def pin_exponential_f32_fill(orc):
     assert (np.abs(e[nz] - ref[nz]) / np.spacing(ref[nz].astype(np.float32))).max() <= 0.505
 
 
+def _cos2pi_reference(m):
+    """cos(2 pi m 2^-23) in binary64 after the same exact reduction (quadrant
+    and g in turns), so that its relative error stays near 2^-52 also next
+    to the zeros of the cosine."""
+    q = m >> 21
+    g = (m & 0x1FFFFF).astype(np.float64) * 2.0 ** -23
+    base = np.where(q % 2 == 0, np.cos(2 * np.pi * g), np.sin(2 * np.pi * g))
+    return np.where((q == 1) | (q == 2), -base, base)
+
+
+def pin_cos2pi_exhaustive(orc):
+    """The precise normal's own cos(2 pi u) on all 2^23 grid angles: within
+    0.95 ulp of the binary64 cosine (measured 0.90), exact at u = 0, 1/4, 1/2
+    and 3/4, and symmetric, cos(2 pi u) = cos(2 pi (1 - u)) bit for bit
+    wherever both sides reduce alike (all but the octant boundaries)."""
+    m = np.arange(1 << 23, dtype=np.uint32)
+    c = orc.cos2pi_array(m)
+    ref = _cos2pi_reference(m)
+    assert np.max(np.abs(ref - np.cos(2 * np.pi * m.astype(np.float64) * 2.0 ** -23))) < 1e-15
+    nz = ref != 0
+    ulp = np.spacing(np.abs(ref[nz]).astype(np.float32)).astype(np.float64)
+    assert np.max(np.abs(c[nz].astype(np.float64) - ref[nz]) / ulp) <= 0.95
+    assert c[0] == 1 and c[1 << 22] == -1 and c[1 << 21] == 0 and c[3 << 21] == 0
+    mm = m[1:]
+    f = mm & 0x1FFFFF
+    ok = (f != 0) & (f != 0x100000)
+    assert np.array_equal(c[mm[ok]].view(np.uint32), c[((1 << 23) - mm[ok])].view(np.uint32))
+
+
+def pin_cos2pi_coefficients(orc):
+    """The Taylor coefficients (2 pi)^n / n! with the series' signs, each the
+    binary32 rounding of the value (within half an ulp), and the hi + lo pairs
+    of 2 pi and -(2 pi)^2/2 within 2^-44 relative."""
+    k = orc.cos2pi_coefficients().astype(np.float64)
+    tp = 2 * math.pi
+    exact = {2: -tp ** 3 / 6, 3: tp ** 5 / 120, 4: -tp ** 7 / 5040, 5: tp ** 9 / 362880,
+             8: tp ** 4 / 24, 9: -tp ** 6 / 720, 10: tp ** 8 / 40320, 11: -tp ** 10 / 3628800}
+    for i, v in exact.items():
+        assert abs(k[i] - v) <= 0.5000001 * float(np.spacing(np.float32(abs(v)))), i
+    assert abs(k[0] + k[1] - tp) <= 2.0 ** -44 * tp and k[0] == np.float32(tp)
+    assert abs(k[6] + k[7] + tp * tp / 2) <= 2.0 ** -44 * tp * tp / 2 and k[6] == np.float32(-tp * tp / 2)
+
+
+def pin_randn_precise(orc):
+    """The precise f32 normal against randn's binary64 value on the same
+    counters: within 2.5 ulp (measured 2.40; the fast f32 path is held to
+    4e-6 (1 + |z|)), zero where u0 = 0, and normal moments."""
+    n = 1 << 22
+    z = orc.fill_randn_precise(7, 0, n).astype(np.float64)
+    ref = orc.fill_randn(7, 0, n)
+    nz = ref != 0
+    ulp = np.spacing(np.abs(ref[nz]).astype(np.float32)).astype(np.float64)
+    assert np.max(np.abs(z[nz] - ref[nz]) / ulp) <= 2.5
+    assert np.all(z[~nz] == 0)
+    _normal_stats(z)
+
+
 # ---------------------------------------------------------------- dropout --
 def pin_dropout(orc):
     """Phobos 'Random numbers', dropout: where(uniform >= p, x / (1 - p), 0)
@@ -576,6 +633,7 @@ def pin_slice_invariant(orc):
         lambda f, m, idx=None: orc.fill_randn_paired(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_exponential_f32(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_exponential_f32_own(9, f, m, idx),
+        lambda f, m, idx=None: orc.fill_randn_precise(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_exponential_f64(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_u32(9, f, m, idx),
         lambda f, m, idx=None: orc.fill_u64(9, f, m, idx),
@@ -606,6 +664,7 @@ ALL_PINS = [
     pin_below_distributions, pin_ranges_wrap, pin_randn_special_angles,
     pin_randn_tail_end, pin_randn_distribution, pin_randn_paired, pin_exponentials,
     pin_neglog_f32_exhaustive, pin_neglog_f32_maps_back, pin_neglog_f32_table, pin_exponential_f32_fill,
+    pin_cos2pi_exhaustive, pin_cos2pi_coefficients, pin_randn_precise,
     pin_dropout, pin_zexp_zlog,
     pin_zig_table_published, pin_zig_table_invariants, pin_zig_miss_rate,
     pin_normal_f64_distribution, pin_zig_wedge_acceptance, pin_slice_invariant,
