@@ -109,6 +109,8 @@ def next_specs():
     return [
         F("normal_f32_pairs", "float32", 4, 0, "fill_kernel<GenNormalF32Pairs>", "normal_f32.cu",
           lambda r, o, f, s: r.rng_fill_normal_f32_pairs(W.NORMAL_SEED, f, o, s)),
+        F("normal_f32_precise", "float32", 4, 0, "fill_kernel<GenNormalF32Precise>", "normal_f32.cu",
+          lambda r, o, f, s: r.rng_fill_normal_f32_precise(W.NORMAL_SEED, f, o, s)),
         F("exponential_f32", "float32", 4, 0, "fill_kernel<GenExpF32>", "exponential.cu",
           lambda r, o, f, s: r.rng_fill_exponential_f32(W.NORMAL_SEED, f, o, s)),
         F("exponential_f64", "float64", 8, 0, "fill_kernel<GenExpF64>", "exponential.cu",
@@ -272,6 +274,7 @@ def oracle_calls(orc, n_sample: int):
         "dropout_fwd_p0.5": drop(x, 0.5),
         "dropout_bwd_p0.5": drop(dy, 0.5),
         "normal_f32_pairs": lambda first, off, n: orc.fill_randn_paired(W.NORMAL_SEED, first + off, n),
+        "normal_f32_precise": lambda first, off, n: orc.fill_randn_precise(W.NORMAL_SEED, first + off, n),
         "exponential_f32": lambda first, off, n: orc.fill_exponential_f32_own(W.NORMAL_SEED, first + off, n),
         "exponential_f64": lambda first, off, n: orc.fill_exponential_f64(W.NORMAL_SEED, first + off, n),
         "u8": lambda first, off, n: orc.fill_u8(W.UNIFORM_SEED, first + off, n),

@@ -47,6 +47,7 @@ _FILL_SIGS = {
     "rng_fill_i64_range": [_u32, _u32, _sz, _i64, _u64, _p, _p],
     "rng_fill_normal_f32": [_u32, _u32, _sz, _p, _p],
     "rng_fill_normal_f32_pairs": [_u32, _u32, _sz, _p, _p],
+    "rng_fill_normal_f32_precise": [_u32, _u32, _sz, _p, _p],
     "rng_fill_exponential_f32": [_u32, _u32, _sz, _p, _p],
     "rng_fill_exponential_f64": [_u32, _u32, _sz, _p, _p],
     "rng_fill_normal_f64": [_u32, _u32, _sz, _p, _p],
@@ -180,6 +181,10 @@ def rng_fill_normal_f32(seed, first_counter, out, stream=None):
 
 def rng_fill_normal_f32_pairs(seed, first_counter, out, stream=None):
     return _fill("rng_fill_normal_f32_pairs", "f32", seed, first_counter, out, stream)
+
+
+def rng_fill_normal_f32_precise(seed, first_counter, out, stream=None):
+    return _fill("rng_fill_normal_f32_precise", "f32", seed, first_counter, out, stream)
 
 
 def rng_fill_exponential_f32(seed, first_counter, out, stream=None):

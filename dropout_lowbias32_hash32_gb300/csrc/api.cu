@@ -268,6 +268,14 @@ rng_status rng_fill_normal_f32_pairs(uint32_t seed, uint32_t first_counter, size
     });
 }
 
+rng_status rng_fill_normal_f32_precise(uint32_t seed, uint32_t first_counter, size_t n, float *out, void *stream)
+{
+    const uint32_t key = seed_key(seed);
+    return fill("rng_fill_normal_f32_precise", first_counter, n, out, [&](uint32_t c, uint32_t len, float *o) {
+        return launch_fill_normal_f32_precise(key, c, len, o, RNG_STREAM(stream));
+    });
+}
+
 rng_status rng_fill_exponential_f32(uint32_t seed, uint32_t first_counter, size_t n, float *out, void *stream)
 {
     const uint32_t key = seed_key(seed);

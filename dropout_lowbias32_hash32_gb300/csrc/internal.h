@@ -84,6 +84,7 @@ cudaError_t launch_fill_i64_range(const Below64Args &a, int64_t low, uint32_t fi
 
 cudaError_t launch_fill_normal_f32(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
 cudaError_t launch_fill_normal_f32_pairs(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
+cudaError_t launch_fill_normal_f32_precise(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
 cudaError_t launch_fill_exponential_f32(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s);
 cudaError_t launch_fill_exponential_f64(uint32_t key, uint32_t first, uint32_t n, double *out, cudaStream_t s);
 

@@ -58,7 +58,23 @@ struct GenNormalF32Pairs {
     }
 };
 
+// The precise variant: randn's definition to a few ulp (lowbias32::randn_precise:
+// the own binary32 -ln(1 - u0) and cos(2 pi u1), an IEEE square root), an
+// opt-in fill with its own values (tandem-sycl "Design", Normals: a precise
+// f32 Box-Muller as a build option).
+struct GenNormalF32Precise {
+    using T = float;
+    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
+    uint32_t key;
+    __device__ T operator()(uint32_t c) const { return lowbias32::randn_precise(lowbias32::Key{key}, c); }
+};
+
 }  // namespace
+
+cudaError_t launch_fill_normal_f32_precise(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s)
+{
+    return launch_fill(GenNormalF32Precise{key}, out, first, n, s);
+}
 
 cudaError_t launch_fill_normal_f32_pairs(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s)
 {

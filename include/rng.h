@@ -150,6 +150,17 @@ rng_status rng_fill_normal_f32(uint32_t seed, uint32_t first_counter, size_t n, 
 rng_status rng_fill_normal_f32_pairs(uint32_t seed, uint32_t first_counter, size_t n, float *out,
                                      void *stream);
 
+/* Precise f32 normal: randn's definition (u0 = uniform(seed, 2 c_i), u1 =
+ * uniform(seed, 2 c_i + 1), z = sqrt(-2 ln(1 - u0)) cos(2 pi u1)) evaluated
+ * in binary32 to a few ulp: the library's own -ln(1 - u0) (within 0.5035 ulp)
+ * and cos(2 pi u1) (within 0.90 ulp), an IEEE square root, so out[i] is
+ * within 2.5 ulp of the exact value and reproducible bit for bit.  An opt-in
+ * variant with its own values: tandem-sycl "Design", section Normals, keeps a
+ * precise f32 Box-Muller as a build option beside the default float normal.
+ * rng_fill_normal_f32 is faster and within 4e-6 (1 + |z|). */
+rng_status rng_fill_normal_f32_precise(uint32_t seed, uint32_t first_counter, size_t n, float *out,
+                                       void *stream);
+
 /* out[i] = standard normal from the 1024-layer Marsaglia-Tsang ziggurat on
  * the 64-bit draw D64(seed, c_i) (tandem-sycl "Design", section Normals).
  * Layer j = w & 1023, sign = bit 10, magnitude x = (w >> 11) 2^-53 X[j]

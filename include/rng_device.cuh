@@ -14,7 +14,8 @@
 // A kernel that gives element e the counter first + e draws exactly what
 // the corresponding fill writes: dropout() is bit-identical to
 // rng_dropout_fwd, uniform() to rng_fill_f32, draw32() to rng_fill_u32;
-// randn() is the value rng_fill_normal_f32 writes.  The page's advice holds:
+// randn() is the value rng_fill_normal_f32 writes, randn_precise() the value
+// rng_fill_normal_f32_precise writes.  The page's advice holds:
 // use each element's flat index as its counter, and give different uses of
 // one seed disjoint counters (randn reads the uniforms at 2c and 2c + 1).
 //
@@ -223,6 +224,52 @@ __device__ __forceinline__ float neg_log_grid(uint32_t m)
 
 // -ln(1 - u) for u = uniform(k, c), by neg_log_grid; in [0, 23 ln 2].
 __device__ __forceinline__ float exponential(Key k, uint32_t c) { return neg_log_grid(draw32(k, c) & 0x7FFFFFu); }
+
+// ---- precise normal --------------------------------------------------------------
+
+namespace detail {
+#include "lowbias32_cos2pi.inc"
+}  // namespace detail
+
+// cos(2 pi m 2^-23) for a 23-bit m in binary32, the library's own: the
+// quadrant q = m >> 21 and g = (m mod 2^21) 2^-23 in [0, 1/4) are exact, and
+// cos(2 pi (q/4 + g)) is cos g, -sin g, -cos g or sin g (angles in turns);
+// above g = 1/8 the complement 1/4 - g (exact) swaps sin and cos.  On x <= 1/8
+// the Taylor series of sin(2 pi x) to x^9 and cos(2 pi x) to x^10 with
+// binary32 coefficients, the leading ones hi + lo.  Within 0.90 ulp of the
+// exact cosine on all 2^23 inputs; exact at the quarter turns.
+__device__ __forceinline__ float cos2pi_grid(uint32_t m)
+{
+    const uint32_t q = m >> 21;
+    const uint32_t f = m & 0x1FFFFFu;
+    const bool swap = f > 0x100000u;
+    const float x = __fmul_rn(detail::small_uint_to_float(swap ? 0x200000u - f : f), 0x1p-23f);  // exact
+    const float x2 = __fmul_rn(x, x);
+    float p = __fmaf_rn(x2, detail::kCos2PiS9, detail::kCos2PiS7);
+    p = __fmaf_rn(x2, p, detail::kCos2PiS5);
+    p = __fmaf_rn(x2, p, detail::kCos2PiS3);
+    p = __fmaf_rn(x2, p, detail::kCos2PiS1Lo);
+    const float sin_x = __fmaf_rn(x, detail::kCos2PiS1Hi, __fmul_rn(x, p));
+    float c = __fmaf_rn(x2, detail::kCos2PiC10, detail::kCos2PiC8);
+    c = __fmaf_rn(x2, c, detail::kCos2PiC6);
+    c = __fmaf_rn(x2, c, detail::kCos2PiC4);
+    const float t = __fmul_rn(x2, __fmaf_rn(x2, c, detail::kCos2PiC2Lo));
+    const float cos_x = __fadd_rn(1.0f, __fmaf_rn(x2, detail::kCos2PiC2Hi, t));
+    const float v = ((q & 1u) != 0u) != swap ? sin_x : cos_x;
+    return (q == 1u || q == 2u) ? -v : v;
+}
+
+// randn's definition (the uniforms at 2c and 2c + 1, cosine branch) evaluated
+// in binary32 to a few ulp: sqrt(2 neg_log_grid(u0)) cos2pi_grid(u1) with an
+// IEEE square root; within 2.5 ulp of the exact value (tandem-sycl "Design",
+// Normals: a precise f32 Box-Muller beside the default float normal).  Not
+// the value randn() gives, which is held to 4e-6 (1 + |z|).
+__device__ __forceinline__ float randn_precise(Key k, uint32_t c)
+{
+    const Words w = draw64_words(k, c);  // the draws at 2c and 2c + 1
+    const float e = neg_log_grid(w.hi & 0x7FFFFFu);
+    return __fmul_rn(__fsqrt_rn(__fadd_rn(e, e)), cos2pi_grid(w.lo & 0x7FFFFFu));
+}
 
 // ---- dropout ------------------------------------------------------------------
 

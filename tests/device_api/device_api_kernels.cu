@@ -7,7 +7,7 @@
 namespace {
 
 __global__ void draw_kernel(uint32_t seed, uint32_t first, uint32_t n, uint32_t *d32, uint64_t *d64, float *u,
-                            float *z, float *ex)
+                            float *z, float *ex, float *zp)
 {
     const lowbias32::Key k = lowbias32::make_key(seed);
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
@@ -17,15 +17,16 @@ __global__ void draw_kernel(uint32_t seed, uint32_t first, uint32_t n, uint32_t 
         u[i] = lowbias32::uniform(k, c);
         z[i] = lowbias32::randn(k, c);
         ex[i] = lowbias32::exponential(k, c);
+        zp[i] = lowbias32::randn_precise(k, c);
     }
 }
 
 }  // namespace
 
 extern "C" int device_api_draws(uint32_t seed, uint32_t first, uint32_t n, uint32_t *d32, uint64_t *d64, float *u,
-                                float *z, float *ex)
+                                float *z, float *ex, float *zp)
 {
-    draw_kernel<<<256, 256>>>(seed, first, n, d32, d64, u, z, ex);
+    draw_kernel<<<256, 256>>>(seed, first, n, d32, d64, u, z, ex, zp);
     return static_cast<int>(cudaDeviceSynchronize());
 }
 
@@ -60,6 +61,19 @@ __global__ void neglog_kernel(const uint32_t *m, float *out, uint32_t n)
 extern "C" int device_api_neglog(const uint32_t *m, float *out, uint32_t n)
 {
     neglog_kernel<<<1024, 256>>>(m, out, n);
+    return static_cast<int>(cudaDeviceSynchronize());
+}
+
+// The header's own cos(2 pi m 2^-23) on given 23-bit inputs (cos2pi_grid).
+__global__ void cos2pi_kernel(const uint32_t *m, float *out, uint32_t n)
+{
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        out[i] = lowbias32::cos2pi_grid(m[i] & 0x7FFFFFu);
+}
+
+extern "C" int device_api_cos2pi(const uint32_t *m, float *out, uint32_t n)
+{
+    cos2pi_kernel<<<1024, 256>>>(m, out, n);
     return static_cast<int>(cudaDeviceSynchronize());
 }
 

@@ -38,8 +38,9 @@ def devlib():
                         "-o", so + ".tmp"], check=True)
         os.replace(so + ".tmp", so)
     lib = C.CDLL(so)
-    lib.device_api_draws.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32] + [C.c_void_p] * 5
+    lib.device_api_draws.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32] + [C.c_void_p] * 6
     lib.device_api_neglog.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32]
+    lib.device_api_cos2pi.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32]
     lib.device_api_dropout_rows.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32, C.c_uint32, C.c_float, C.c_uint32,
                                             C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_float)]
     lib.device_api_host_hash32.argtypes = [C.c_uint32]
@@ -79,6 +80,28 @@ def test_header_neglog_on_every_input(devlib, orc):
     assert np.array_equal(out.cpu().numpy().view(np.uint32), orc.neglog_array(m).view(np.uint32))
 
 
+def test_header_cos2pi_coefficients_match_the_oracle(orc):
+    """The header's generated coefficients (gen_cos2pi_coefficients.py, mpmath)
+    equal the oracle's own (binary128 in C), in the oracle's order."""
+    import re
+    txt = open(os.path.join(ROOT, "include", "lowbias32_cos2pi.inc")).read()
+    vals = dict(re.findall(r"constexpr float (kCos2Pi\w+) = ([^;]+);", txt))
+    names = ["S1Hi", "S1Lo", "S3", "S5", "S7", "S9", "C2Hi", "C2Lo", "C4", "C6", "C8", "C10"]
+    got = np.array([float.fromhex(vals["kCos2Pi" + k][:-1]) for k in names])
+    assert np.array_equal(got, orc.cos2pi_coefficients().astype(np.float64))
+
+
+@pytest.mark.gpu
+def test_header_cos2pi_on_every_input(devlib, orc):
+    """cos2pi_grid on all 2^23 inputs equals the oracle's own cosine, bit for bit."""
+    import torch
+    m = np.arange(1 << 23, dtype=np.uint32)
+    mg = torch.from_numpy(m.view(np.int32)).cuda()
+    out = torch.empty(m.size, dtype=torch.float32, device="cuda")
+    assert devlib.device_api_cos2pi(mg.data_ptr(), out.data_ptr(), m.size) == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), orc.cos2pi_array(m).view(np.uint32))
+
+
 def test_header_hash_on_the_host_matches_the_oracle(devlib, orc):
     for x in (0, 1, 2, 0x9E3779B9, U32 - 1, 123456789):
         assert devlib.device_api_host_hash32(x) == orc.hash32(x)
@@ -96,8 +119,9 @@ def test_header_draws_match_the_oracle_and_the_fills(devlib, orc, first):
     u = torch.empty(n, dtype=torch.float32, device="cuda")
     z = torch.empty(n, dtype=torch.float32, device="cuda")
     ex = torch.empty(n, dtype=torch.float32, device="cuda")
+    zp = torch.empty(n, dtype=torch.float32, device="cuda")
     assert devlib.device_api_draws(seed, first, n, d32.data_ptr(), d64.data_ptr(), u.data_ptr(), z.data_ptr(),
-                                   ex.data_ptr()) == 0
+                                   ex.data_ptr(), zp.data_ptr()) == 0
     assert np.array_equal(d32.cpu().numpy().view(np.uint32), orc.fill_u32(seed, first, n))
     assert np.array_equal(d64.cpu().numpy().view(np.uint64), orc.fill_u64(seed, first, n))
     assert np.array_equal(u.cpu().numpy().view(np.uint32), orc.fill_f32(seed, first, n).view(np.uint32))
@@ -111,6 +135,9 @@ def test_header_draws_match_the_oracle_and_the_fills(devlib, orc, first):
                           orc.fill_exponential_f32_own(seed, first, n).view(np.uint32))
     lib_ex = rng.rng_fill_exponential_f32(seed, first, torch.empty(n, dtype=torch.float32, device="cuda"))
     assert torch.equal(lib_ex.view(torch.int32), ex.view(torch.int32))
+    assert np.array_equal(zp.cpu().numpy().view(np.uint32), orc.fill_randn_precise(seed, first, n).view(np.uint32))
+    lib_zp = rng.rng_fill_normal_f32_precise(seed, first, torch.empty(n, dtype=torch.float32, device="cuda"))
+    assert torch.equal(lib_zp.view(torch.int32), zp.view(torch.int32))
 
 
 CANDIDATES = (1, 2, 4, 8, 16, 32)

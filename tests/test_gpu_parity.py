@@ -94,6 +94,8 @@ def fills(rng, torch, orc):
                       lambda f, n: orc.fill_i64_range(4, f, -500, 1000, n)),
         "normal_f64": (lambda o, f: rng.rng_fill_normal_f64(7, f, o), t.float64,
                        lambda f, n: orc.fill_normal_f64(7, f, n)),
+        "normal_f32_precise": (lambda o, f: rng.rng_fill_normal_f32_precise(7, f, o), t.float32,
+                               lambda f, n: orc.fill_randn_precise(7, f, n)),
         "exponential_f32": (lambda o, f: rng.rng_fill_exponential_f32(13, f, o), t.float32,
                             lambda f, n: orc.fill_exponential_f32_own(13, f, n)),
         "exponential_f64": (lambda o, f: rng.rng_fill_exponential_f64(13, f, o), t.float64,
@@ -112,7 +114,7 @@ def fills(rng, torch, orc):
 FILL_NAMES = ["u32", "u64", "f32", "f64", "u32_below_1000", "u32_below_2^32-2", "u32_below_2^31+1",
               "u64_below_1000", "u64_below_2^64-2", "u64_below_2^63+1", "i32_range", "i32_range_wrap",
               "i64_range32", "i64_range", "normal_f64", "u8", "u16", "f16", "bool", "exponential_f32",
-              "exponential_f64"]
+              "exponential_f64", "normal_f32_precise"]
 
 
 @pytest.mark.parametrize("name", FILL_NAMES)
