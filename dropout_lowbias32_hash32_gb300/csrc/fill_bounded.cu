@@ -64,11 +64,67 @@ __device__ __forceinline__ uint64_t below64(const Below64Args &a, uint32_t c)
     return __umul64hi(x, a.bound);
 }
 
+// The candidate for counter c without its rejection test's branch: the
+// value if accepted, and `reject` set when the low word is below the
+// threshold (then the element must take its retries).
+__device__ __forceinline__ uint32_t below32_candidate(const Below32Args &a, uint32_t c, bool &reject)
+{
+    const uint64_t m = static_cast<uint64_t>(draw32(a.key, c)) * a.bound;
+    reject |= static_cast<uint32_t>(m) < a.threshold;
+    return static_cast<uint32_t>(m >> 32);
+}
+
+// x b as (high, low) 64-bit words.  A bound below 2^32 (the same for every
+// thread of a launch, so the branch does not diverge) needs only the two
+// 32 x 32 -> 64 products of x's halves: x b = (x_hi b) 2^32 + x_lo b.
+__device__ __forceinline__ uint64_t mul_64(uint64_t x, uint64_t bound, uint64_t &low)
+{
+    if ((bound >> 32) == 0) {
+        const uint32_t b = static_cast<uint32_t>(bound);
+        const uint64_t p_lo = static_cast<uint64_t>(static_cast<uint32_t>(x)) * b;
+        const uint64_t p_hi = static_cast<uint64_t>(static_cast<uint32_t>(x >> 32)) * b;
+        const uint64_t mid = (p_lo >> 32) + static_cast<uint32_t>(p_hi);  // < 2^33
+        low = (mid << 32) | static_cast<uint32_t>(p_lo);
+        return (p_hi >> 32) + (mid >> 32);
+    }
+    low = x * bound;
+    return __umul64hi(x, bound);
+}
+
+__device__ __forceinline__ uint64_t below64_candidate(const Below64Args &a, uint32_t c, bool &reject)
+{
+    uint64_t low;
+    const uint64_t high = mul_64(draw64(a.key, c), a.bound, low);
+    reject |= low < a.threshold;
+    return high;
+}
+
+// A 16-byte vector of a bounded fill: every element's candidate and one
+// branch on the OR of their rejection tests (rare: about 4 (2^w mod b) / 2^w
+// per vector), whose slow path recomputes the vector element by element with
+// retries.  The same values as the per-element function.
+template <class Gen, class T = typename Gen::T>
+__device__ __forceinline__ Vec16<T> bounded_vec(const Gen &gen, uint32_t c0)
+{
+    constexpr uint32_t kPer = Vec16<T>::kPer;
+    Vec16<T> x;
+    bool reject = false;
+#pragma unroll
+    for (uint32_t k = 0; k < kPer; ++k) x.v[k] = gen.candidate(c0 + k, reject);
+    if (__builtin_expect(reject, 0)) {
+#pragma unroll
+        for (uint32_t k = 0; k < kPer; ++k) x.v[k] = gen(c0 + k);
+    }
+    return x;
+}
+
 struct GenBelow32 {
     using T = uint32_t;
     static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     Below32Args a;
     __device__ T operator()(uint32_t c) const { return below32(a, c); }
+    __device__ T candidate(uint32_t c, bool &reject) const { return below32_candidate(a, c, reject); }
+    __device__ Vec16<T> vec(uint32_t c0) const { return bounded_vec(*this, c0); }
 };
 
 struct GenBelow64 {
@@ -76,6 +132,8 @@ struct GenBelow64 {
     static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     Below64Args a;
     __device__ T operator()(uint32_t c) const { return below64(a, c); }
+    __device__ T candidate(uint32_t c, bool &reject) const { return below64_candidate(a, c, reject); }
+    __device__ Vec16<T> vec(uint32_t c0) const { return bounded_vec(*this, c0); }
 };
 
 // low + below, wrapped in two's complement (unsigned addition, then the
@@ -89,6 +147,11 @@ struct GenI32Range {
     {
         return static_cast<int32_t>(static_cast<uint32_t>(low) + below32(a, c));
     }
+    __device__ T candidate(uint32_t c, bool &reject) const
+    {
+        return static_cast<int32_t>(static_cast<uint32_t>(low) + below32_candidate(a, c, reject));
+    }
+    __device__ Vec16<T> vec(uint32_t c0) const { return bounded_vec(*this, c0); }
 };
 
 struct GenI64Range32 {
@@ -99,6 +162,11 @@ struct GenI64Range32 {
     {
         return static_cast<int64_t>(static_cast<uint64_t>(low) + below32(a, c));
     }
+    __device__ T candidate(uint32_t c, bool &reject) const
+    {
+        return static_cast<int64_t>(static_cast<uint64_t>(low) + below32_candidate(a, c, reject));
+    }
+    __device__ Vec16<T> vec(uint32_t c0) const { return bounded_vec(*this, c0); }
 };
 
 struct GenI64Range {
@@ -110,6 +178,11 @@ struct GenI64Range {
     {
         return static_cast<int64_t>(static_cast<uint64_t>(low) + below64(a, c));
     }
+    __device__ T candidate(uint32_t c, bool &reject) const
+    {
+        return static_cast<int64_t>(static_cast<uint64_t>(low) + below64_candidate(a, c, reject));
+    }
+    __device__ Vec16<T> vec(uint32_t c0) const { return bounded_vec(*this, c0); }
 };
 
 }  // namespace
