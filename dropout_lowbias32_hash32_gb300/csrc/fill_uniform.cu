@@ -47,9 +47,11 @@ __device__ __noinline__ double scaled_small_u53(uint32_t lo)
     return __dmul_rn(__uint2double_rn(lo >> 11), 0x1p-53);
 }
 
-__device__ __forceinline__ double scaled_u53_to_double(Words w)
+// The normalising conversion alone; `small` is set when the high word is
+// zero (then the value must come from scaled_small_u53).
+__device__ __forceinline__ double scaled_u53_candidate(Words w, bool &small)
 {
-    if (__builtin_expect(w.hi == 0, 0)) return scaled_small_u53(w.lo);
+    small |= w.hi == 0;
     const uint32_t lo = w.lo & ~0x7FFu;
     const uint32_t z = __clz(w.hi);
     const uint32_t a_hi = __funnelshift_l(lo, w.hi, z);  // (hi:lo) << z, high word
@@ -59,11 +61,32 @@ __device__ __forceinline__ double scaled_u53_to_double(Words w)
     return __hiloint2double(static_cast<int>(sig_hi + ((1021u - z) << 20)), static_cast<int>(sig_lo));
 }
 
+__device__ __forceinline__ double scaled_u53_to_double(Words w)
+{
+    bool small = false;
+    const double x = scaled_u53_candidate(w, small);
+    return __builtin_expect(small, 0) ? scaled_small_u53(w.lo) : x;
+}
+
 struct GenF64 {
     using T = double;
     static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     uint32_t key;
     __device__ T operator()(uint32_t c) const { return scaled_u53_to_double(draw64_words(key, c)); }
+    // both elements of a 16-byte vector, one branch on a zero high word
+    __device__ Vec16<T> vec(uint32_t c0) const
+    {
+        const Words w0 = draw64_words(key, c0), w1 = draw64_words(key, c0 + 1u);
+        bool small = false;
+        Vec16<T> x;
+        x.v[0] = scaled_u53_candidate(w0, small);
+        x.v[1] = scaled_u53_candidate(w1, small);
+        if (__builtin_expect(small, 0)) {
+            x.v[0] = scaled_u53_to_double(w0);
+            x.v[1] = scaled_u53_to_double(w1);
+        }
+        return x;
+    }
 };
 
 }  // namespace
