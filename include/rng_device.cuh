@@ -130,21 +130,22 @@ __device__ __forceinline__ float box_muller_radius(uint32_t d0)
     const float one_plus_u0 = __uint_as_float(0x3F800000u | (d0 & 0x7FFFFFu));
     const float u0 = one_plus_u0 - 1.0f;
     const float v = 2.0f - one_plus_u0;
-    float series = __fmaf_rn(u0, 0.2f, 0.25f);
-    series = __fmaf_rn(u0, series, 0.333333343f);
-    series = __fmaf_rn(u0, series, 0.5f);
+    float series = __fmaf_rn(u0, 0.4f, 0.5f);      // 2 (1 + u/2 + u^2/3 + u^3/4 + u^4/5)
+    series = __fmaf_rn(u0, series, 0.666666687f);
     series = __fmaf_rn(u0, series, 1.0f);
-    const float small = (2.0f * u0) * series;      // -2 ln(1 - u0), u0 < 2^-5
+    series = __fmaf_rn(u0, series, 2.0f);
+    const float small = u0 * series;               // -2 ln(1 - u0), u0 < 2^-5
     const float large = -1.38629436f * lg2_approx(v);  // -2 ln 2 log2(1 - u0)
     return sqrt_approx((d0 & 0x7C0000u) ? large : small);
 }
 
-// The angle 2 pi (u1 - 1/2) in [-pi, pi) from the draw d1 at 2c + 1, with
-// u1 - 1/2 = (1 + u1) - 3/2 exact: cos(2 pi u1) = -cos(angle),
-// sin(2 pi u1) = -sin(angle).
+// The angle 2 pi (u1 - 1/2) in [-pi, pi) from the draw d1 at 2c + 1, as
+// (1 + u1) 2 pi - 3 pi in one fused multiply-add (within 5e-7 of the exact
+// angle): cos(2 pi u1) = -cos(angle), sin(2 pi u1) = -sin(angle).
 __device__ __forceinline__ float box_muller_angle(uint32_t d1)
 {
-    return (__uint_as_float(0x3F800000u | (d1 & 0x7FFFFFu)) - 1.5f) * 6.28318530717958647692f;
+    return __fmaf_rn(__uint_as_float(0x3F800000u | (d1 & 0x7FFFFFu)), 6.28318530717958647692f,
+                     -9.42477796076937971538f);
 }
 }  // namespace detail
 
