@@ -313,6 +313,38 @@ def test_normal_f64_streams_share_the_miss_list(rng, torch, orc):
         _assert_equal(f"stream fill {k}", _host(o), orc.fill_normal_f64(7, k * n, n))
 
 
+def test_normal_f64_from_concurrent_host_threads(rng, torch, orc):
+    """Four host threads, each on its own stream, fill concurrently (the C
+    calls release the GIL); sizes grow so that the shared miss list is
+    reallocated while other threads' fills are queued.  Every output equals
+    the oracle's."""
+    import threading
+    sizes = [1 << 16, 1 << 20, 3 << 20, 1 << 22]
+    results, errors = {}, []
+
+    def work(t):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for k, n in enumerate(sizes[t:] + sizes[:t]):
+                    o = torch.empty(n, dtype=torch.float64, device="cuda")
+                    rng.rng_fill_normal_f64(100 + t, k * 977, o)
+                    results[(t, k)] = (n, o)
+            s.synchronize()
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for (t, k), (n, o) in sorted(results.items()):
+        _assert_equal(f"thread {t} fill {k}", _host(o), orc.fill_normal_f64(100 + t, k * 977, n))
+
+
 def test_launch_counts(rng, torch):
     o32 = torch.empty(1 << 16, dtype=torch.float32, device="cuda")
     o64 = torch.empty(1 << 16, dtype=torch.float64, device="cuda")
