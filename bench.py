@@ -537,30 +537,73 @@ def write_ceiling(rng, torch, buf, stream, reps):
 
 
 def run_e2e(rng, torch, specs, outs, host_inputs, x, dy, n, stream, barrier, dist, dev, steps, world):
-    """The step through the C ABI with host buffers: each dropout input is
-    copied from pinned host memory, each fill's output is copied back to
-    pinned host memory, inside the timed region."""
-    host_out = torch.empty(n * 8, dtype=torch.uint8, pin_memory=True)
+    """The step through the C ABI with host buffers, inside the timed region:
+    each dropout input is copied from pinned host memory and every fill's
+    output is copied back to pinned host memory.  Three streams overlap the
+    two copy directions with the fills: the fills run on `stream`,
+    host-to-device copies on one side stream and device-to-host copies on
+    another; outputs and dropout inputs are double-buffered on the device,
+    and events keep a fill from overwriting a buffer before its copy out has
+    read it (and a copy in from overwriting an input a dropout still reads)."""
+    del outs, x, dy  # the pipelined step has its own double buffers
     host_x, host_dy = host_inputs
-    h2d = d2h = 0
+    dtypes = {"int32": torch.int32, "float32": torch.float32, "int64": torch.int64, "float64": torch.float64,
+              "x": torch.float32, "dy": torch.float32}
+    dev_out = [torch.empty(n * 8, dtype=torch.uint8, device=dev) for _ in range(2)]
+    host_out = [torch.empty(n * 8, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    dev_in = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def event(s):
+        e = torch.cuda.Event()
+        e.record(s)
+        return e
+
+    def one_step(state):
+        h2d = d2h = 0
+        for spec in specs:
+            b = state["k"] % 2
+            if state["out_free"][b] is not None:
+                stream.wait_event(state["out_free"][b])
+            out = dev_out[b].view(dtypes[spec.kind])[:n]
+            if spec.kind in ("x", "dy"):
+                ib = state["ki"] % 2
+                if state["in_free"][ib] is not None:
+                    s_in.wait_event(state["in_free"][ib])
+                with torch.cuda.stream(s_in):
+                    dev_in[ib].copy_(host_x if spec.kind == "x" else host_dy, non_blocking=True)
+                stream.wait_event(event(s_in))
+                spec.call(rng, (dev_in[ib], out), 0, stream)
+                state["in_free"][ib] = event(stream)
+                state["ki"] += 1
+                h2d += n * 4
+            else:
+                spec.call(rng, out, 0, stream)
+            nbytes = n * spec.written
+            s_out.wait_event(event(stream))
+            with torch.cuda.stream(s_out):
+                host_out[b][:nbytes].copy_(dev_out[b][:nbytes], non_blocking=True)
+            state["out_free"][b] = event(s_out)
+            state["k"] += 1
+            d2h += nbytes
+        return h2d, d2h
+
+    state = {"k": 0, "ki": 0, "out_free": [None, None], "in_free": [None, None]}
+    one_step(state)  # untimed warm-up
+    torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     t0.record(stream)
+    start = event(stream)
+    s_in.wait_event(start)
+    s_out.wait_event(start)
+    h2d = d2h = 0
     for _ in range(steps):
-        for spec in specs:
-            if spec.kind in ("x", "dy"):
-                src, dst = (host_x, x) if spec.kind == "x" else (host_dy, dy)
-                dst.copy_(src, non_blocking=True)
-                h2d += n * 4
-                spec.call(rng, outs[spec.kind], 0, stream)
-                res = outs[spec.kind][1]
-            else:
-                res = outs[spec.kind]
-                spec.call(rng, res, 0, stream)
-            nbytes = n * spec.written
-            host_out[:nbytes].copy_(res.view(torch.uint8).view(-1)[:nbytes], non_blocking=True)
-            d2h += nbytes
+        a, b = one_step(state)
+        h2d, d2h = h2d + a, d2h + b
+    stream.wait_event(event(s_out))
+    stream.wait_event(event(s_in))
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -571,7 +614,8 @@ def run_e2e(rng, torch, specs, outs, host_inputs, x, dy, n, stream, barrier, dis
         ms = float(t.item())
     value = sum(n * s.written for s in specs) * world * steps / (ms / 1e3) / GIB
     return {"value": round(value, 1), "unit": "GiB/s", "h2d_bytes_per_step": h2d // steps,
-            "d2h_bytes_per_step": d2h // steps, "steps": steps}
+            "d2h_bytes_per_step": d2h // steps, "steps": steps,
+            "pipelining": "fills, host-to-device and device-to-host copies on three streams"}
 
 
 # --------------------------------------------------------- reference arm ---
