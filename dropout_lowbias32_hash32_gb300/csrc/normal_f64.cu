@@ -5,11 +5,13 @@
 // tandem-sycl "Design", section Normals: one 64-bit draw per element; 0.43 %
 // of draws miss the fast path and continue on a substream keyed by the
 // draw's global index, so a fill cut at any element equals the whole fill;
-// the table pass queues a block's misses locally and appends them to a device
-// list with one atomic add; the second kernel takes one miss per thread and,
-// if the list overflowed, walks the whole fill again; the layer table lives in
-// global memory (constant memory serialises lanes that read different
-// layers); the fast path makes no calls.
+// misses are queued locally and appended to a device list with one atomic
+// add (here: per-warp queues in shared memory, flushed 32 entries at a time);
+// the second kernel takes one miss per thread and, if the list overflowed,
+// walks the whole fill again; the layer table is not in constant memory,
+// which serialises lanes that read different layers (here: the table pass
+// reads 8 bank-staggered shared-memory replicas, the slow path global
+// memory through L1); the fast path makes no calls.
 //
 // Misses of the base layer (1.3 % of misses) need two logarithms and a
 // division, the others (wedges) one exponential: the table pass keeps them in
