@@ -75,6 +75,21 @@ CASES = [
      lambda orc, f, idx: orc.fill_i64_range(3, f, W.LOW, 1000, idx=idx)),
     ("normal_f64", "float64", lambda r, o, f: r.rng_fill_normal_f64(W.NORMAL_SEED, f, o),
      lambda orc, f, idx: orc.fill_normal_f64(W.NORMAL_SEED, f, idx=idx)),
+    # the fills beyond the step, which bench.py also times at this size
+    ("exponential_f32", "float32", lambda r, o, f: r.rng_fill_exponential_f32(W.NORMAL_SEED, f, o),
+     lambda orc, f, idx: orc.fill_exponential_f32_own(W.NORMAL_SEED, f, idx=idx)),
+    ("exponential_f64", "float64", lambda r, o, f: r.rng_fill_exponential_f64(W.NORMAL_SEED, f, o),
+     lambda orc, f, idx: orc.fill_exponential_f64(W.NORMAL_SEED, f, idx=idx)),
+    ("normal_f32_precise", "float32", lambda r, o, f: r.rng_fill_normal_f32_precise(W.NORMAL_SEED, f, o),
+     lambda orc, f, idx: orc.fill_randn_precise(W.NORMAL_SEED, f, idx=idx)),
+    ("u8", "uint8", lambda r, o, f: r.rng_fill_u8(W.UNIFORM_SEED, f, o),
+     lambda orc, f, idx: orc.fill_u8(W.UNIFORM_SEED, f, idx=idx)),
+    ("u16", "int16", lambda r, o, f: r.rng_fill_u16(W.UNIFORM_SEED, f, o),
+     lambda orc, f, idx: orc.fill_u16(W.UNIFORM_SEED, f, idx=idx).view(np.int16)),
+    ("f16", "float16", lambda r, o, f: r.rng_fill_f16(W.UNIFORM_SEED, f, o),
+     lambda orc, f, idx: orc.fill_f16_bits(W.UNIFORM_SEED, f, idx=idx).view(np.float16)),
+    ("bool", "bool", lambda r, o, f: r.rng_fill_bool(W.UNIFORM_SEED, f, o),
+     lambda orc, f, idx: orc.fill_bool(W.UNIFORM_SEED, f, idx=idx).astype(np.bool_)),
 ]
 
 
@@ -120,6 +135,16 @@ def test_full_size_normal_f32(rng, torch, orc, sample):
     assert abs(zt.var().item() - 1) < 5 * math.sqrt(2 / N)
     assert zt.abs().max().item() <= math.sqrt(-2 * math.log(2.0 ** -23)) * (1 + 1e-6)
     del out, zt
+    torch.cuda.empty_cache()
+
+
+def test_full_size_normal_f32_pairs(rng, torch, orc, sample):
+    out = torch.empty(N, dtype=torch.float32, device="cuda")
+    rng.rng_fill_normal_f32_pairs(W.NORMAL_SEED, 1, out)
+    z = _gather(torch, out, sample).astype(np.float64)
+    ref = orc.fill_randn_paired(W.NORMAL_SEED, 1, idx=sample)
+    assert np.max(np.abs(z - ref) / (1 + np.abs(ref))) <= 4e-6
+    del out
     torch.cuda.empty_cache()
 
 
