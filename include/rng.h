@@ -32,7 +32,11 @@
  *     synchronisation, as for any CUDA kernel.  RNG_ENOMEM reports a failed
  *     allocation of the library's own per-device ziggurat miss list.
  *     rng_last_error() gives a message for the calling thread's last error.
- *   - Every call is thread-safe.
+ *   - Every call is thread-safe, except that calls of
+ *     rng_fill_normal_f64_noalloc whose work overlaps on the GPU race (see
+ *     there).
+ *   - The fills other than the two f64 normals keep no device state: their
+ *     launches can be captured into a CUDA graph and replayed.
  *   - A fill cut at any element equals the whole fill: filling [a, b) with
  *     first_counter + a gives elements a..b-1 of the fill from first_counter.
  */
