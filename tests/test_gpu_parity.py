@@ -18,7 +18,10 @@ U32 = 1 << 32
 FIRSTS = (0, 1, 3, U32 - 5)
 # 3 waves of the u32 fill (152 SMs x 8 blocks x 256 threads x 4 elements) + a ragged tail
 BIG = 3 * 152 * 8 * 256 * 4 + 13
-SMALL = (1, 2, 3, 5, 15, 16, 17, 31, 33, 1000, 4095, 4096, 4097, 65537)
+# around the vector width and around one block's run of every generator
+# (256 threads x 4 or 8 vectors x 16/sizeof(T) elements: 2048 .. 16384)
+SMALL = (1, 2, 3, 5, 15, 16, 17, 31, 33, 1000, 2047, 2048, 2049, 4095, 4096, 4097, 8191, 8192, 8193,
+         16383, 16384, 16385, 65537)
 
 
 @pytest.fixture(scope="module")
@@ -294,6 +297,20 @@ def test_normal_f64_miss_count(rng, torch, orc):
     assert got == want
     p = 0.0042766
     assert abs(got - p * n) < 5 * math.sqrt(p * n)
+
+
+@pytest.mark.parametrize("name", ["u32", "u64_below_1000", "i64_range", "normal_f64", "exponential_f32", "u8",
+                                  "normal_f32_precise"])
+def test_resume_from_a_counter(rng, torch, orc, name):
+    """Checkpoint and resume: a stream position is (seed, next counter), so a
+    fill done in pieces, each started at first_counter + its offset, equals
+    the fill done at once (the ziggurat's misses included)."""
+    gpu, dtype, _ = fills(rng, torch, orc)[name]
+    n, first = 1 << 20, U32 - 70000  # the counters wrap inside the fill
+    whole = _host(gpu(_out(torch, dtype, n, 0), first))
+    cuts = [0, 12345, 12346, 500001, n]
+    parts = [_host(gpu(_out(torch, dtype, b - a, a % 3), (first + a) % U32)) for a, b in zip(cuts, cuts[1:])]
+    assert np.array_equal(_bits(np.concatenate(parts)), _bits(whole))
 
 
 def test_normal_f64_streams_share_the_miss_list(rng, torch, orc):
