@@ -81,6 +81,8 @@ _SIGS = {
     "orc_fill_randn_precise": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_cos2pi_fill": (None, [_p, _sz, _p]),
     "orc_cos2pi_coefficients": (None, [_p]),
+    "orc_neglog64_fill": (None, [_p, _sz, _p]),
+    "orc_neglog64_table": (None, [_p, _p, _p, _p, _p]),
     "orc_neglog_table": (None, [_p, _p, _p, _p]),
     "orc_randn_paired": (_f64, [_u32, _u32]),
     "orc_fill_normal_f64": (None, [_u32, _u32, _sz, _p, _p]),
@@ -303,6 +305,26 @@ class Oracle:
         out = np.empty(12, np.float32)
         self.lib.orc_cos2pi_coefficients(_ptr(out))
         return out
+
+    def neglog64_array(self, m):
+        """-ln(1 - m 2^-53) in binary64 by the own fixed-point log, for 53-bit integers m."""
+        m = np.ascontiguousarray(m, dtype=np.uint64)
+        if m.size and int(m.max()) >= 1 << 53:
+            raise ValueError("m must be below 2^53")
+        out = np.empty(m.size, np.float64)
+        self.lib.orc_neglog64_fill(_ptr(m), m.size, _ptr(out))
+        return out
+
+    def neglog64_table(self):
+        """I_j (257), ln inv_j at 2^96 as Python ints (257), ln 2 at 2^96, and the
+        Taylor coefficients c[1..8] at 2^62."""
+        inv = np.empty(257, np.int32)
+        hi, lo = np.empty(257, np.int64), np.empty(257, np.uint64)
+        ln2, coef = np.empty(2, np.int64), np.empty(9, np.int64)
+        self.lib.orc_neglog64_table(_ptr(inv), _ptr(hi), _ptr(lo), _ptr(ln2), _ptr(coef))
+        lninv = [(int(h) << 64) + int(l) for h, l in zip(hi, lo)]
+        return ([int(x) for x in inv], lninv, (int(ln2[0]) << 64) + (int(ln2[1]) & ((1 << 64) - 1)),
+                [int(c) for c in coef])
 
     def neglog_table(self):
         """The own log's table: inv, hi, lo (257 binary32 each) and (ln2_hi, ln2_lo)."""

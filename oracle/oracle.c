@@ -338,8 +338,9 @@ double orc_zlog(double x)
 
 /* ------------------------------------------------------------------------ */
 /* Exponentials [Tandem-D, section Exponentials]: -ln(1 - u).  READING: the   */
-/* f32 fill on the f32 uniform (evaluated here in binary64, not rounded), the */
-/* f64 fill on the f64 uniform through this file's own logarithm.            */
+/* f32 fill on the f32 uniform (its binary64 value here; the fill's own       */
+/* binary32 log below), the f64 fill on the f64 uniform through this file's   */
+/* own fixed-point logarithm (further below).                                */
 /* ------------------------------------------------------------------------ */
 
 double orc_exponential_f32(uint32_t seed, uint32_t counter)
@@ -527,10 +528,102 @@ float orc_exponential_f32_own(uint32_t seed, uint32_t counter)
     return orc_neglog_f32(orc_draw32(seed, counter) & 8388607u);
 }
 
+/* -ln(1 - m 2^-53) in binary64 by the library's own fixed-point logarithm,
+ * integer arithmetic only (GB300's FP64 pipe is 1/64 of its FP32 rate).
+ * READING (the pages' f64 logarithm is not printed; their exponentials need
+ * only an own, reproducible log): with V = 2^53 - m (1 - u = V 2^-53 exactly),
+ *   V = 2^k M, M in [1, 2), E = 53 - k, so -ln(1 - u) = E ln 2 - ln M;
+ *   j = round((M - 1) 256), I_j = 256/(256 + j) rounded to 8 significant
+ *   bits times 256 (the reciprocal inv_j = I_j / 256 of the f32 log), and
+ *   r = M inv_j - 1 = (V I_j - 2^(k+8)) 2^-(k+8), an exact integer ratio,
+ *   |r| < 1.5 2^-8 (Tang 1990, as the f32 log);
+ *   log1p(r) = r S(r), S(r) = 1 - r/2 + r^2/3 - ... - r^7/8 (Taylor; the next
+ *   term is below 2^-62 of the result), S by Horner in 64-bit fixed point
+ *   (scale 2^62, each product's high 64 bits shifted down, i.e. floored),
+ *   r S exact in 128 bits (scale 2^132);
+ *   -ln(1 - u) = E ln 2 + ln inv_j - r S, with E ln2 + ln inv_j at scale
+ *   2^96 (ln 2 and ln inv_j each rounded once to the nearest multiple of
+ *   2^-96) and r S floored to it; where E ln 2 + ln inv_j is exactly 0 (E = 1,
+ *   inv_j = 1/2) the value is -r S itself, at scale 2^132;
+ *   the positive fixed-point value rounded once to binary64, to nearest even.
+ * Within 0.5005 ulp of the exact value on the inputs tried. */
+static int32_t nl64_i[257];
+static __int128 nl64_lninv[257], nl64_ln2;
+static int64_t nl64_c[9]; /* c[k] = (-1)^(k+1) / k at 2^62, k = 1 .. 8 */
+static int nl64_ready;
+
+static __int128 nl64_round96(quad v) { return (__int128)Q_RINT(v * (quad)79228162514264337593543950336.0); } /* 2^96 */
+
+static void nl64_init(void)
+{
+    if (nl64_ready) return;
+    for (int j = 0; j <= 256; ++j) {
+        nl64_i[j] = (int32_t)(round_to_bits(256.0 / (256.0 + j), 8) * 256.0);
+        nl64_lninv[j] = nl64_round96(Q_LOG((quad)nl64_i[j] / 256));
+    }
+    nl64_ln2 = nl64_round96(Q_LOG((quad)2));
+    for (int k = 1; k <= 8; ++k) {
+        quad ck = (quad)4611686018427387904.0 / k; /* 2^62 / k */
+        nl64_c[k] = (int64_t)Q_RINT(k % 2 ? ck : -ck);
+    }
+    nl64_ready = 1;
+}
+
+/* the positive integer y times 2^-scale, rounded to the nearest binary64 */
+static double nl64_to_double(unsigned __int128 y, int scale)
+{
+    int n = 0;
+    for (unsigned __int128 t = y; t; t >>= 1) ++n; /* bit length */
+    uint64_t mant;
+    int shift = n - 53;
+    if (shift <= 0) {
+        mant = (uint64_t)(y << -shift);
+    } else {
+        mant = (uint64_t)(y >> shift);
+        unsigned __int128 rest = y - ((unsigned __int128)mant << shift);
+        unsigned __int128 half = (unsigned __int128)1 << (shift - 1);
+        if (rest > half || (rest == half && (mant & 1))) ++mant;
+    }
+    return ldexp((double)mant, shift - scale); /* mant <= 2^53: exact in binary64 */
+}
+
+double orc_neglog64(uint64_t m) /* m < 2^53 */
+{
+    nl64_init();
+    if (m == 0) return 0.0;
+    uint64_t V = (1ull << 53) - m;
+    int k = 63 - __builtin_clzll(V);
+    int E = 53 - k;
+    uint64_t Vn = V << (63 - k);
+    uint32_t j = (uint32_t)(((Vn - (1ull << 63)) + (1ull << 54)) >> 55);
+    int64_t R = (int64_t)(V * (uint64_t)nl64_i[j]) - (int64_t)(1ull << (k + 8));
+    int64_t r = R * (int64_t)(1ull << (62 - k)); /* r 2^70, exact */
+    int64_t S = nl64_c[8];
+    for (int t = 7; t >= 1; --t) S = nl64_c[t] + (int64_t)((((__int128)r * S) >> 64) >> 6); /* floor((r S) 2^-70) */
+    __int128 P = (__int128)r * S; /* log1p(r) 2^132, exact */
+    if (E == 1 && nl64_i[j] == 128) return nl64_to_double((unsigned __int128)(-P), 132);
+    __int128 y = (__int128)E * nl64_ln2 + nl64_lninv[j] - (P >> 36);
+    return nl64_to_double((unsigned __int128)y, 96);
+}
+
+/* The f64 exponential fill: -ln(1 - u) on the f64 uniform u = (D64 >> 11)
+ * 2^-53, through the fixed-point logarithm above. */
 double orc_exponential_f64(uint32_t seed, uint32_t counter)
 {
-    double v = 1.0 - orc_uniform_f64(seed, counter);
-    return 0.0 - orc_zlog(v);
+    return orc_neglog64(orc_draw64(seed, counter) >> 11);
+}
+
+void orc_neglog64_table(int32_t *inv256, int64_t *lninv_hi, uint64_t *lninv_lo, int64_t *ln2, int64_t *coef)
+{
+    nl64_init();
+    for (int j = 0; j <= 256; ++j) {
+        inv256[j] = nl64_i[j];
+        lninv_hi[j] = (int64_t)(nl64_lninv[j] >> 64);
+        lninv_lo[j] = (uint64_t)nl64_lninv[j];
+    }
+    ln2[0] = (int64_t)(nl64_ln2 >> 64);
+    ln2[1] = (int64_t)(uint64_t)nl64_ln2;
+    for (int k = 0; k <= 8; ++k) coef[k] = nl64_c[k];
 }
 
 /* ------------------------------------------------------------------------ */
@@ -801,6 +894,11 @@ void orc_cos2pi_fill(const uint32_t *m, size_t n, float *out)
 void orc_neglog_fill(const uint32_t *m, size_t n, float *out)
 {
     for (size_t i = 0; i < n; ++i) out[i] = orc_neglog_f32(m[i]);
+}
+
+void orc_neglog64_fill(const uint64_t *m, size_t n, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_neglog64(m[i]);
 }
 
 void orc_fill_exponential_f64(uint32_t seed, uint32_t first, size_t n, const uint64_t *idx, double *out)

@@ -473,6 +473,91 @@ def pin_randn_precise(orc):
     _normal_stats(z)
 
 
+def _neglog64_sample():
+    """53-bit inputs: edge values, every bin edge of the log's table at the two
+    largest exponents, and random values of every bit length."""
+    g = np.random.default_rng(9)
+    ms = [0, 1, 2, 3, (1 << 52) - 1, 1 << 52, (1 << 52) + 1, (1 << 53) - 2, (1 << 53) - 1]
+    for k in (52, 51):  # V = 2^53 - m in [2^k, 2^(k+1)): bin j starts at M = 1 + (j - 1/2)/256
+        for j in range(1, 257):
+            edge = (1 << 53) - (((2 * j - 1) << k) // 512 + (1 << k))
+            ms += [edge + d for d in (-1, 0, 1) if 0 <= edge + d < 1 << 53]
+    bits = g.integers(1, 54, 1 << 18)
+    ms += [int(x) >> (64 - int(b)) for x, b in zip(g.integers(0, 1 << 63, 1 << 18, dtype=np.uint64) << np.uint64(1),
+                                                 bits)]
+    return np.unique(np.array(ms, dtype=np.uint64))
+
+
+def pin_neglog64_accuracy(orc):
+    """The f64 exponential's own fixed-point log against -log1p(-u) in x87
+    extended precision (64-bit significand; on x86-64 numpy's longdouble):
+    within 0.5025 ulp on the sample (measured 0.5015, part of it the
+    reference's own error), and against mpmath at 50 digits on a subset: within
+    0.5006 ulp.  +0 at m = 0, monotone in m, 53 ln 2 at the top."""
+    ms = _neglog64_sample()
+    y = orc.neglog64_array(ms)
+    assert y[0] == 0 and not np.signbit(y[0])
+    assert np.all(np.diff(y) >= 0)
+    assert y[-1] == np.float64(53 * math.log(2)) or abs(y[-1] - 53 * math.log(2)) <= np.spacing(53 * math.log(2))
+    if np.finfo(np.longdouble).nmant >= 63:
+        u = ms.astype(np.longdouble) / np.longdouble(2) ** 53
+        ref = -np.log1p(-u)
+        nz = ref > 0
+        err = np.abs(y[nz].astype(np.longdouble) - ref[nz]) / np.spacing(ref[nz].astype(np.float64))
+        assert float(err.max()) <= 0.5025
+    import mpmath as mp
+    mp.mp.dps = 50
+    sub = ms[:: max(1, ms.size // 3000)]
+    ys = orc.neglog64_array(sub)
+    worst = 0.0
+    for m, v in zip(sub, ys):
+        if m == 0:
+            continue
+        ref = -mp.log1p(-mp.mpf(int(m)) / 2 ** 53)
+        worst = max(worst, float(abs(mp.mpf(float(v)) - ref) / (mp.mpf(2) ** (math.frexp(float(ref))[1] - 53))))
+    assert worst <= 0.5006
+
+
+def pin_neglog64_table(orc):
+    """The fixed-point log's constants against their definitions: I_j = 256/(256
+    + j) rounded to 8 significant bits, times 256 (exact rationals); ln(I_j /
+    256) and ln 2 each the nearest integer multiple of 2^-96 (mpmath, 60
+    digits), so that E ln 2 + ln inv_j cancels exactly where inv_j = 1/2; the
+    Taylor coefficients (-1)^(k+1)/k at 2^62."""
+    import mpmath as mp
+    from fractions import Fraction
+    mp.mp.dps = 60
+    inv, lninv, ln2, coef = orc.neglog64_table()
+    for j in range(257):
+        x = Fraction(256 * 256, 256 + j)  # 2^16/(256 + j), to be rounded to an integer of 8 significant bits
+        q, rem = divmod(x.numerator, x.denominator)
+        if 2 * rem > x.denominator or (2 * rem == x.denominator and q % 2):
+            q += 1
+        if j == 0:
+            q = 256  # 2^16/256 = 256, exact
+        assert inv[j] == q and 128 <= q <= 256, j
+        assert lninv[j] == int(mp.nint(mp.log(mp.mpf(inv[j]) / 256) * mp.mpf(2) ** 96)), j
+    assert ln2 == int(mp.nint(mp.log(2) * mp.mpf(2) ** 96))
+    assert lninv[255] == lninv[256] == -ln2 and inv[255] == inv[256] == 128
+    for k in range(1, 9):
+        assert coef[k] == int(mp.nint(mp.mpf((-1) ** (k + 1)) / k * mp.mpf(2) ** 62)), k
+
+
+def pin_exponential_f64_fill(orc):
+    """The f64 exponential fill is the fixed-point log of the draw's top 53
+    bits: within 0.5025 ulp of -log1p(-u) in extended precision on the same
+    counters, with mean 1 and variance 1."""
+    n = 1 << 20
+    e = orc.fill_exponential_f64(13, 7, n)
+    u64 = orc.fill_u64(13, 7, n) >> np.uint64(11)
+    assert np.array_equal(e.view(np.uint64), orc.neglog64_array(u64).view(np.uint64))
+    if np.finfo(np.longdouble).nmant >= 63:
+        ref = -np.log1p(-(u64.astype(np.longdouble) / np.longdouble(2) ** 53))
+        nz = ref > 0
+        assert float((np.abs(e[nz].astype(np.longdouble) - ref[nz]) / np.spacing(ref[nz].astype(np.float64))).max()) <= 0.5025
+    assert abs(e.mean() - 1) < 5 / math.sqrt(n) and abs(e.var() - 1) < 5 * math.sqrt(8 / n)
+
+
 # ---------------------------------------------------------------- dropout --
 def pin_dropout(orc):
     """Phobos 'Random numbers', dropout: where(uniform >= p, x / (1 - p), 0)
@@ -665,6 +750,7 @@ ALL_PINS = [
     pin_randn_tail_end, pin_randn_distribution, pin_randn_paired, pin_exponentials,
     pin_neglog_f32_exhaustive, pin_neglog_f32_maps_back, pin_neglog_f32_table, pin_exponential_f32_fill,
     pin_cos2pi_exhaustive, pin_cos2pi_coefficients, pin_randn_precise,
+    pin_neglog64_accuracy, pin_neglog64_table, pin_exponential_f64_fill,
     pin_dropout, pin_zexp_zlog,
     pin_zig_table_published, pin_zig_table_invariants, pin_zig_miss_rate,
     pin_normal_f64_distribution, pin_zig_wedge_acceptance, pin_slice_invariant,
