@@ -9,12 +9,11 @@
 //        lowbias32::neg_log_grid of include/rng_device.cuh (a table-driven
 //        binary32 logarithm, within 0.5035 ulp of the exact value on every
 //        input); e in [0, 23 ln 2].
-//   f64: e = 0 - zlog(1 - u), u = (D64 >> 11) 2^-53; 1 - u is exact and
-//        zlog is the fixed IEEE sequence of f64_math.cuh, so the value is
-//        reproducible bit for bit; e in [0, 53 ln 2].
-// GB300 retires 2 FP64 operations per SM and cycle; the f64 logarithm
-// (a division and a degree-11 series, about 26 FP64 operations) makes that
-// fill FP64-bound at a small fraction of the HBM rate.
+//   f64: e = -ln(1 - u), u = (D64 >> 11) 2^-53, by neglog64 of f64_math.cuh:
+//        a fixed-point logarithm in 64- and 128-bit integer arithmetic
+//        (GB300 retires 2 FP64 operations per SM and cycle, 1/64 of its FP32
+//        rate), within 0.5015 ulp and reproducible bit for bit; e in
+//        [0, 53 ln 2].
 #include "f64_math.cuh"
 #include "fill_kernel.cuh"
 #include "hash32.cuh"
@@ -29,28 +28,13 @@ struct GenExpF32 {
     __device__ T operator()(uint32_t c) const { return lowbias32::exponential(lowbias32::Key{key}, c); }
 };
 
-// (w >> 11) 2^-53 exactly, from integer operations (as the f64 uniform fill)
-__device__ __forceinline__ double u53_exact(Words w)
-{
-    if (w.hi == 0) return __dmul_rn(__uint2double_rn(w.lo >> 11), 0x1p-53);
-    const uint32_t lo = w.lo & ~0x7FFu;
-    const uint32_t z = __clz(w.hi);
-    const uint32_t a_hi = __funnelshift_l(lo, w.hi, z);
-    const uint32_t a_lo = lo << z;
-    const uint32_t sig_hi = a_hi >> 11;
-    const uint32_t sig_lo = __funnelshift_r(a_lo, a_hi, 11);
-    return __hiloint2double(static_cast<int>(sig_hi + ((1021u - z) << 20)), static_cast<int>(sig_lo));
-}
-
+// -ln(1 - u) on the f64 uniform u = (D64 >> 11) 2^-53, by the fixed-point
+// logarithm of f64_math.cuh (integer arithmetic only).
 struct GenExpF64 {
     using T = double;
-    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
+    static constexpr uint32_t kVectorsPerThread = 2;  // a long body: keep the unrolled code small
     uint32_t key;
-    __device__ T operator()(uint32_t c) const
-    {
-        const double v = __dsub_rn(1.0, u53_exact(draw64_words(key, c)));  // exact, in (0, 1]
-        return __dsub_rn(0.0, zlog(v));
-    }
+    __device__ T operator()(uint32_t c) const { return neglog64(draw64(key, c) >> 11); }
 };
 
 }  // namespace

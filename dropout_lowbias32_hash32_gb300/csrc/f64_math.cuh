@@ -1,8 +1,9 @@
-// f64_math.cuh -- the library's own binary64 exp and log: fixed sequences of
-// IEEE operations (+, -, *, /, fma with explicit rounding intrinsics), so a
-// second implementation performing the same operations in the same order
-// returns the same bits on any IEEE machine.  Used by the ziggurat's slow
-// path and by the f64 exponential fill.
+// f64_math.cuh -- the library's own binary64 functions, each a fixed
+// sequence of exact integer or IEEE operations (+, -, *, /, fma with explicit
+// rounding intrinsics), so that a second implementation performing the same
+// operations returns the same bits on any IEEE machine: zexp and zlog for the
+// ziggurat's slow path, and neglog64, the fixed-point -ln(1 - u) of the f64
+// exponential fill.
 #pragma once
 
 #include <cstdint>
@@ -70,6 +71,83 @@ __device__ __forceinline__ double zlog(double x)
     const double log_m = __fma_rn(__dmul_rn(two_s, s2), p, two_s);
     const double de = static_cast<double>(e);
     return __fma_rn(de, ZK_LN2_HIGH, __fma_rn(de, ZK_LN2_LOW, log_m));
+}
+
+// ---- the f64 exponential's fixed-point logarithm ----------------------------
+
+#include "neglog64_table.inc"
+
+// y 2^-scale for a positive 128-bit integer y >= 2^53 (as it is on every path
+// of neglog64), rounded to the nearest binary64, ties to even: y is shifted
+// left until its leading one is bit 127 (z places), the significand is then
+// bits 127 .. 75, the rounding bit bit 74 and the sticky bits 73 .. 0; the
+// value is mant 2^(75 - z - scale).  Same result as rounding y 2^-scale
+// directly, on 64-bit halves only.
+__device__ __forceinline__ double fixed_to_double(unsigned __int128 y, int scale)
+{
+    const unsigned long long hi = static_cast<unsigned long long>(y >> 64);
+    const unsigned long long lo = static_cast<unsigned long long>(y);
+    unsigned long long H, L;
+    int z;
+    if (hi) {
+        z = __clzll(static_cast<long long>(hi));
+        H = z ? (hi << z) | (lo >> (64 - z)) : hi;
+        L = lo << z;
+    } else {
+        z = 64 + __clzll(static_cast<long long>(lo));
+        H = lo << (z - 64);
+        L = 0;
+    }
+    unsigned long long mant = H >> 11;
+    const unsigned long long round = (H >> 10) & 1ull;
+    const unsigned long long sticky = ((H & 0x3FFull) | L) != 0ull;
+    mant += round & (sticky | (mant & 1ull));
+    // mant in [2^52, 2^53]: biased exponent 1023 + 52 + 75 - z - scale,
+    // written one lower because the significand's leading one (or a rounding
+    // carry to 2^53) adds one to the field
+    const long long e = 1022 + 52 + 75 - z - scale;
+    return __longlong_as_double(static_cast<long long>((static_cast<unsigned long long>(e) << 52) + mant));
+}
+
+// -ln(1 - m 2^-53) for m < 2^53 in integer arithmetic only (tandem-sycl
+// "Design", Exponentials: an own reproducible logarithm).  V = 2^53 - m = 2^k M,
+// E = 53 - k; bin j = round((M - 1) 256) with I_j = 256 inv_j; r = M inv_j - 1 =
+// (V I_j - 2^(k+8)) 2^-(k+8) exactly, |r| < 1.5 2^-8; log1p(r) = r S(r), S to
+// r^7 by Horner at scale 2^62 (products floored), r S exact in 128 bits (scale
+// 2^132); -ln(1 - u) = E ln 2 + ln inv_j - r S at scale 2^96, or -r S itself
+// where E ln 2 + ln inv_j is exactly 0 (E = 1, inv_j = 1/2); rounded once to
+// binary64.  Within 0.5015 ulp of the exact value.
+__device__ __forceinline__ double neglog64(unsigned long long m)
+{
+    if (m == 0) return 0.0;
+    const unsigned long long V = (1ull << 53) - m;
+    const int k = 63 - __clzll(static_cast<long long>(V));
+    const int E = 53 - k;
+    const unsigned long long Vn = V << (63 - k);
+    const unsigned j = static_cast<unsigned>(((Vn - (1ull << 63)) + (1ull << 54)) >> 55);
+    const ulonglong2 row = __ldg(&kNegLog64Table[j]);
+    const unsigned inv = static_cast<unsigned>(row.y >> 48);
+    const long long R = static_cast<long long>(V * inv - (1ull << (k + 8)));
+    const long long r = static_cast<long long>(static_cast<unsigned long long>(R) << (62 - k));  // r 2^70, exact
+    long long S = kNegLog64C8;  // S = C8, then C_t + floor((r S) 2^-70) for t = 7 .. 1
+    S = kNegLog64C7 + (__mul64hi(r, S) >> 6);
+    S = kNegLog64C6 + (__mul64hi(r, S) >> 6);
+    S = kNegLog64C5 + (__mul64hi(r, S) >> 6);
+    S = kNegLog64C4 + (__mul64hi(r, S) >> 6);
+    S = kNegLog64C3 + (__mul64hi(r, S) >> 6);
+    S = kNegLog64C2 + (__mul64hi(r, S) >> 6);
+    S = kNegLog64C1 + (__mul64hi(r, S) >> 6);
+    const __int128 P = static_cast<__int128>(r) * S;                           // log1p(r) 2^132
+    const long long lninv_hi = static_cast<long long>(row.y << 16) >> 16;        // the signed 48-bit field
+    // two's complement of lninv_hi 2^64 + low: the high word's 64-bit pattern above the low word
+    const __int128 lninv = static_cast<__int128>(
+        (static_cast<unsigned __int128>(static_cast<unsigned long long>(lninv_hi)) << 64) | row.x);
+    const __int128 ln2 = static_cast<__int128>(
+        (static_cast<unsigned __int128>(static_cast<unsigned long long>(kNegLog64Ln2Hi)) << 64) | kNegLog64Ln2Lo);
+    // -r S itself (scale 2^132) where E ln 2 + ln inv_j is exactly 0, else the sum at 2^96
+    const bool exact_small = E == 1 && inv == 128u;
+    const __int128 y = exact_small ? -P : static_cast<__int128>(E) * ln2 + lninv - (P >> 36);
+    return fixed_to_double(static_cast<unsigned __int128>(y), exact_small ? 132 : 96);
 }
 
 }  // namespace rngk

@@ -340,7 +340,9 @@ __global__ void eval_f64_kernel(int which, const double *in, double *out, uint32
 {
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-        out[i] = which ? zlog(in[i]) : zexp(in[i]);
+        out[i] = which == 2 ? neglog64(static_cast<unsigned long long>(__double_as_longlong(in[i])) &
+                                      0x1FFFFFFFFFFFFFull)
+                 : which ? zlog(in[i]) : zexp(in[i]);
 }
 
 // Expected misses of n elements (p = 0.42766 %, of which the base layer's

@@ -259,9 +259,11 @@ rng_status rng_debug_last_miss_count(uint64_t *count);
  * devices and threads. */
 uint64_t rng_debug_launch_count(void);
 
-/* Evaluates the normal_f64 slow path's own exp (which = 0) or log (which = 1)
- * on the device: out[i] = f(in[i]) for i < n, in and out device arrays of
- * doubles.  For checking the slow path layer by layer. */
+/* Evaluates the library's own binary64 functions on the device, out[i] =
+ * f(in[i]) for i < n (in and out device arrays of doubles): the normal_f64
+ * slow path's exp (which = 0) or log (which = 1), or (which = 2) the f64
+ * exponential's fixed-point -ln(1 - m 2^-53) with m the low 53 bits of
+ * in[i]'s bit pattern.  For checking those functions on chosen inputs. */
 rng_status rng_debug_eval_f64(int which, const double *in, double *out, size_t n, void *stream);
 
 /* A measurement aid with no counterpart on the pages: the write ceiling the

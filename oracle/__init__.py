@@ -317,7 +317,7 @@ class Oracle:
 
     def neglog64_table(self):
         """I_j (257), ln inv_j at 2^96 as Python ints (257), ln 2 at 2^96, and the
-        Taylor coefficients c[1..8] at 2^62."""
+        Horner constants 1/k: at 2^62 for k = 1 .. 5, at 2^31 for k = 6 .. 8."""
         inv = np.empty(257, np.int32)
         hi, lo = np.empty(257, np.int64), np.empty(257, np.uint64)
         ln2, coef = np.empty(2, np.int64), np.empty(9, np.int64)

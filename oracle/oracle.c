@@ -537,19 +537,24 @@ float orc_exponential_f32_own(uint32_t seed, uint32_t counter)
  *   bits times 256 (the reciprocal inv_j = I_j / 256 of the f32 log), and
  *   r = M inv_j - 1 = (V I_j - 2^(k+8)) 2^-(k+8), an exact integer ratio,
  *   |r| < 1.5 2^-8 (Tang 1990, as the f32 log);
- *   log1p(r) = r S(r), S(r) = 1 - r/2 + r^2/3 - ... - r^7/8 (Taylor; the next
- *   term is below 2^-62 of the result), S by Horner in 64-bit fixed point
- *   (scale 2^62, each product's high 64 bits shifted down, i.e. floored),
- *   r S exact in 128 bits (scale 2^132);
- *   -ln(1 - u) = E ln 2 + ln inv_j - r S, with E ln2 + ln inv_j at scale
- *   2^96 (ln 2 and ln inv_j each rounded once to the nearest multiple of
- *   2^-96) and r S floored to it; where E ln 2 + ln inv_j is exactly 0 (E = 1,
- *   inv_j = 1/2) the value is -r S itself, at scale 2^132;
+ *   log1p(r) = r S(r), S(r) = sum_k (-r)^(k-1) / k for k = 1 .. 8 (Taylor; the
+ *   next term is below 2^-62 of the result).  With a = |r| every Horner value
+ *   S_k = 1/k + (-r) S_(k+1) is positive: S_k = 1/k + a S_(k+1) for r < 0 and
+ *   1/k - a S_(k+1) for r >= 0.  S_8 .. S_6 in 32-bit fixed point (scale
+ *   2^31; those steps need only 2^-26), S_5 .. S_1 in 64-bit fixed point
+ *   (scale 2^62), each product's high part floored; a S exact in 128 bits
+ *   (scale 2^132);
+ *   -ln(1 - u) = E ln 2 + ln inv_j -+ a S (minus for r >= 0), with E ln2 +
+ *   ln inv_j at scale 2^96 (ln 2 and ln inv_j each rounded once to the
+ *   nearest multiple of 2^-96) and a S floored to it; where E ln 2 + ln inv_j
+ *   is exactly 0 (E = 1, inv_j = 1/2, so r < 0) the value is a S itself, at
+ *   scale 2^132;
  *   the positive fixed-point value rounded once to binary64, to nearest even.
  * Within 0.5005 ulp of the exact value on the inputs tried. */
 static int32_t nl64_i[257];
 static __int128 nl64_lninv[257], nl64_ln2;
-static int64_t nl64_c[9]; /* c[k] = (-1)^(k+1) / k at 2^62, k = 1 .. 8 */
+static uint64_t nl64_d64[6]; /* 1/k at 2^62, k = 1 .. 5 */
+static uint32_t nl64_d32[9]; /* 1/k at 2^31, k = 6 .. 8 */
 static int nl64_ready;
 
 static __int128 nl64_round96(quad v) { return (__int128)Q_RINT(v * (quad)79228162514264337593543950336.0); } /* 2^96 */
@@ -562,10 +567,8 @@ static void nl64_init(void)
         nl64_lninv[j] = nl64_round96(Q_LOG((quad)nl64_i[j] / 256));
     }
     nl64_ln2 = nl64_round96(Q_LOG((quad)2));
-    for (int k = 1; k <= 8; ++k) {
-        quad ck = (quad)4611686018427387904.0 / k; /* 2^62 / k */
-        nl64_c[k] = (int64_t)Q_RINT(k % 2 ? ck : -ck);
-    }
+    for (int k = 1; k <= 5; ++k) nl64_d64[k] = (uint64_t)Q_RINT((quad)4611686018427387904.0 / k); /* 2^62 / k */
+    for (int k = 6; k <= 8; ++k) nl64_d32[k] = (uint32_t)Q_RINT((quad)2147483648.0 / k);          /* 2^31 / k */
     nl64_ready = 1;
 }
 
@@ -597,12 +600,23 @@ double orc_neglog64(uint64_t m) /* m < 2^53 */
     uint64_t Vn = V << (63 - k);
     uint32_t j = (uint32_t)(((Vn - (1ull << 63)) + (1ull << 54)) >> 55);
     int64_t R = (int64_t)(V * (uint64_t)nl64_i[j]) - (int64_t)(1ull << (k + 8));
-    int64_t r = R * (int64_t)(1ull << (62 - k)); /* r 2^70, exact */
-    int64_t S = nl64_c[8];
-    for (int t = 7; t >= 1; --t) S = nl64_c[t] + (int64_t)((((__int128)r * S) >> 64) >> 6); /* floor((r S) 2^-70) */
-    __int128 P = (__int128)r * S; /* log1p(r) 2^132, exact */
-    if (E == 1 && nl64_i[j] == 128) return nl64_to_double((unsigned __int128)(-P), 132);
-    __int128 y = (__int128)E * nl64_ln2 + nl64_lninv[j] - (P >> 36);
+    int up = R < 0; /* -r > 0: every Horner term adds */
+    uint64_t a = (uint64_t)(up ? -R : R) << (62 - k); /* |r| 2^70, exact */
+    uint32_t a32 = (uint32_t)(a >> 32);             /* |r| 2^38 */
+    uint32_t S32 = nl64_d32[8];
+    for (int t = 7; t >= 6; --t) {
+        uint32_t p = (uint32_t)(((uint64_t)a32 * S32) >> 38); /* floor(a S 2^-38) at 2^31 */
+        S32 = up ? nl64_d32[t] + p : nl64_d32[t] - p;
+    }
+    uint64_t S = (uint64_t)S32 << 31; /* to 2^62 */
+    for (int t = 5; t >= 1; --t) {
+        uint64_t p = (uint64_t)(((unsigned __int128)a * S) >> 70); /* floor(a S 2^-70) at 2^62 */
+        S = up ? nl64_d64[t] + p : nl64_d64[t] - p;
+    }
+    unsigned __int128 Pm = (unsigned __int128)a * S; /* |log1p(r)| 2^132, exact */
+    if (E == 1 && nl64_i[j] == 128) return nl64_to_double(Pm, 132);
+    __int128 T = (__int128)E * nl64_ln2 + nl64_lninv[j];
+    __int128 y = up ? T + (__int128)(Pm >> 36) : T - (__int128)(Pm >> 36);
     return nl64_to_double((unsigned __int128)y, 96);
 }
 
@@ -623,7 +637,9 @@ void orc_neglog64_table(int32_t *inv256, int64_t *lninv_hi, uint64_t *lninv_lo, 
     }
     ln2[0] = (int64_t)(nl64_ln2 >> 64);
     ln2[1] = (int64_t)(uint64_t)nl64_ln2;
-    for (int k = 0; k <= 8; ++k) coef[k] = nl64_c[k];
+    coef[0] = 0;
+    for (int k = 1; k <= 5; ++k) coef[k] = (int64_t)nl64_d64[k];
+    for (int k = 6; k <= 8; ++k) coef[k] = (int64_t)nl64_d32[k];
 }
 
 /* ------------------------------------------------------------------------ */

@@ -523,7 +523,7 @@ def pin_neglog64_table(orc):
     + j) rounded to 8 significant bits, times 256 (exact rationals); ln(I_j /
     256) and ln 2 each the nearest integer multiple of 2^-96 (mpmath, 60
     digits), so that E ln 2 + ln inv_j cancels exactly where inv_j = 1/2; the
-    Taylor coefficients (-1)^(k+1)/k at 2^62."""
+    Horner constants 1/k, at 2^62 for k <= 5 and at 2^31 for k = 6 .. 8."""
     import mpmath as mp
     from fractions import Fraction
     mp.mp.dps = 60
@@ -540,7 +540,7 @@ def pin_neglog64_table(orc):
     assert ln2 == int(mp.nint(mp.log(2) * mp.mpf(2) ** 96))
     assert lninv[255] == lninv[256] == -ln2 and inv[255] == inv[256] == 128
     for k in range(1, 9):
-        assert coef[k] == int(mp.nint(mp.mpf((-1) ** (k + 1)) / k * mp.mpf(2) ** 62)), k
+        assert coef[k] == int(mp.nint(mp.mpf(2) ** (62 if k <= 5 else 31) / k)), k
 
 
 def pin_exponential_f64_fill(orc):

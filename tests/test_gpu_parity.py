@@ -270,6 +270,18 @@ def test_slow_path_exp_log_bit_exact(rng, torch, orc):
     _assert_equal("zlog", _host(rng.rng_debug_eval_f64(1, torch.from_numpy(x).cuda(), out)), orc.zlog_array(x))
 
 
+def test_f64_fixed_point_log_on_chosen_inputs(rng, torch, orc):
+    """The f64 exponential's fixed-point log on the device, on the oracle pin's
+    inputs (every table bin edge at the two largest exponents, edge values and
+    random inputs of every bit length) and 2^20 more, bit for bit."""
+    import pins
+    g = np.random.default_rng(6)
+    m = np.concatenate([pins._neglog64_sample(), g.integers(0, 1 << 53, 1 << 20, dtype=np.uint64)])
+    out = torch.empty(m.size, dtype=torch.float64, device="cuda")
+    got = _host(rng.rng_debug_eval_f64(2, torch.from_numpy(m.view(np.float64)).cuda(), out))
+    _assert_equal("neglog64", got, orc.neglog64_array(m))
+
+
 def test_normal_f64_miss_list_overflow_walks_the_fill(rng, torch, orc):
     """A list too short for the misses (capacity 0 and 5) sends the second
     kernel through the whole fill: the values must not change."""
