@@ -112,11 +112,13 @@ __device__ __forceinline__ double fixed_to_double(unsigned __int128 y, int scale
 // -ln(1 - m 2^-53) for m < 2^53 in integer arithmetic only (tandem-sycl
 // "Design", Exponentials: an own reproducible logarithm).  V = 2^53 - m = 2^k M,
 // E = 53 - k; bin j = round((M - 1) 256) with I_j = 256 inv_j; r = M inv_j - 1 =
-// (V I_j - 2^(k+8)) 2^-(k+8) exactly, |r| < 1.5 2^-8; log1p(r) = r S(r), S to
-// r^7 by Horner at scale 2^62 (products floored), r S exact in 128 bits (scale
-// 2^132); -ln(1 - u) = E ln 2 + ln inv_j - r S at scale 2^96, or -r S itself
-// where E ln 2 + ln inv_j is exactly 0 (E = 1, inv_j = 1/2); rounded once to
-// binary64.  Within 0.5015 ulp of the exact value.
+// (V I_j - 2^(k+8)) 2^-(k+8) exactly, |r| < 1.5 2^-8; log1p(r) = r S(r), S =
+// sum (-r)^(k-1)/k to k = 8 by Horner on a = |r| (every Horner value positive:
+// S_k = 1/k + a S_(k+1) for r < 0, 1/k - a S_(k+1) otherwise), S_8 .. S_6 in
+// 32-bit fixed point (scale 2^31), S_5 .. S_1 in 64-bit (scale 2^62), products
+// floored; a S exact in 128 bits (scale 2^132); -ln(1 - u) = E ln 2 + ln inv_j
+// -+ a S at scale 2^96, or a S itself where E ln 2 + ln inv_j is exactly 0
+// (E = 1, inv_j = 1/2); rounded once to binary64.  Within 0.5005 ulp.
 __device__ __forceinline__ double neglog64(unsigned long long m)
 {
     if (m == 0) return 0.0;
@@ -128,26 +130,38 @@ __device__ __forceinline__ double neglog64(unsigned long long m)
     const ulonglong2 row = __ldg(&kNegLog64Table[j]);
     const unsigned inv = static_cast<unsigned>(row.y >> 48);
     const long long R = static_cast<long long>(V * inv - (1ull << (k + 8)));
-    const long long r = static_cast<long long>(static_cast<unsigned long long>(R) << (62 - k));  // r 2^70, exact
-    long long S = kNegLog64C8;  // S = C8, then C_t + floor((r S) 2^-70) for t = 7 .. 1
-    S = kNegLog64C7 + (__mul64hi(r, S) >> 6);
-    S = kNegLog64C6 + (__mul64hi(r, S) >> 6);
-    S = kNegLog64C5 + (__mul64hi(r, S) >> 6);
-    S = kNegLog64C4 + (__mul64hi(r, S) >> 6);
-    S = kNegLog64C3 + (__mul64hi(r, S) >> 6);
-    S = kNegLog64C2 + (__mul64hi(r, S) >> 6);
-    S = kNegLog64C1 + (__mul64hi(r, S) >> 6);
-    const __int128 P = static_cast<__int128>(r) * S;                           // log1p(r) 2^132
-    const long long lninv_hi = static_cast<long long>(row.y << 16) >> 16;        // the signed 48-bit field
+    const bool up = R < 0;  // -r > 0: every Horner term adds
+    const unsigned long long a = static_cast<unsigned long long>(up ? -R : R) << (62 - k);  // |r| 2^70
+    const unsigned a32 = static_cast<unsigned>(a >> 32);                                      // |r| 2^38
+    unsigned S32 = kNegLog64D8;
+    unsigned p32 = __umulhi(a32, S32) >> 6;  // floor(a S 2^-38) at 2^31
+    S32 = up ? kNegLog64D7 + p32 : kNegLog64D7 - p32;
+    p32 = __umulhi(a32, S32) >> 6;
+    S32 = up ? kNegLog64D6 + p32 : kNegLog64D6 - p32;
+    unsigned long long S = static_cast<unsigned long long>(S32) << 31;  // to 2^62
+    unsigned long long p = __umul64hi(a, S) >> 6;                        // floor(a S 2^-70) at 2^62
+    S = up ? kNegLog64D5 + p : kNegLog64D5 - p;
+    p = __umul64hi(a, S) >> 6;
+    S = up ? kNegLog64D4 + p : kNegLog64D4 - p;
+    p = __umul64hi(a, S) >> 6;
+    S = up ? kNegLog64D3 + p : kNegLog64D3 - p;
+    p = __umul64hi(a, S) >> 6;
+    S = up ? kNegLog64D2 + p : kNegLog64D2 - p;
+    p = __umul64hi(a, S) >> 6;
+    S = up ? kNegLog64D1 + p : kNegLog64D1 - p;
+    const unsigned __int128 Pm = static_cast<unsigned __int128>(a) * S;  // |log1p(r)| 2^132
+    const long long lninv_hi = static_cast<long long>(row.y << 16) >> 16;  // the signed 48-bit field
     // two's complement of lninv_hi 2^64 + low: the high word's 64-bit pattern above the low word
     const __int128 lninv = static_cast<__int128>(
         (static_cast<unsigned __int128>(static_cast<unsigned long long>(lninv_hi)) << 64) | row.x);
     const __int128 ln2 = static_cast<__int128>(
         (static_cast<unsigned __int128>(static_cast<unsigned long long>(kNegLog64Ln2Hi)) << 64) | kNegLog64Ln2Lo);
-    // -r S itself (scale 2^132) where E ln 2 + ln inv_j is exactly 0, else the sum at 2^96
+    // a S itself (scale 2^132) where E ln 2 + ln inv_j is exactly 0, else the sum at 2^96
     const bool exact_small = E == 1 && inv == 128u;
-    const __int128 y = exact_small ? -P : static_cast<__int128>(E) * ln2 + lninv - (P >> 36);
-    return fixed_to_double(static_cast<unsigned __int128>(y), exact_small ? 132 : 96);
+    const __int128 T = static_cast<__int128>(E) * ln2 + lninv;
+    const __int128 q = static_cast<__int128>(Pm >> 36);
+    const unsigned __int128 y = exact_small ? Pm : static_cast<unsigned __int128>(up ? T + q : T - q);
+    return fixed_to_double(y, exact_small ? 132 : 96);
 }
 
 }  // namespace rngk
