@@ -77,27 +77,19 @@ __device__ __forceinline__ double zlog(double x)
 
 #include "neglog64_table.inc"
 
-// y 2^-scale for a positive 128-bit integer y >= 2^53 (as it is on every path
-// of neglog64), rounded to the nearest binary64, ties to even: y is shifted
+// y 2^-scale for an integer 2^64 <= y < 2^128 (on both paths of neglog64 y is
+// at least 2^79), rounded to the nearest binary64, ties to even: y is shifted
 // left until its leading one is bit 127 (z places), the significand is then
 // bits 127 .. 75, the rounding bit bit 74 and the sticky bits 73 .. 0; the
-// value is mant 2^(75 - z - scale).  Same result as rounding y 2^-scale
+// value is mant 2^(75 - z - scale).  The same result as rounding y 2^-scale
 // directly, on 64-bit halves only.
 __device__ __forceinline__ double fixed_to_double(unsigned __int128 y, int scale)
 {
     const unsigned long long hi = static_cast<unsigned long long>(y >> 64);
     const unsigned long long lo = static_cast<unsigned long long>(y);
-    unsigned long long H, L;
-    int z;
-    if (hi) {
-        z = __clzll(static_cast<long long>(hi));
-        H = z ? (hi << z) | (lo >> (64 - z)) : hi;
-        L = lo << z;
-    } else {
-        z = 64 + __clzll(static_cast<long long>(lo));
-        H = lo << (z - 64);
-        L = 0;
-    }
+    const int z = __clzll(static_cast<long long>(hi));           // 0 .. 63: hi != 0
+    const unsigned long long H = (hi << z) | ((lo >> 1) >> (63 - z));  // (hi:lo) << z, high word
+    const unsigned long long L = lo << z;
     unsigned long long mant = H >> 11;
     const unsigned long long round = (H >> 10) & 1ull;
     const unsigned long long sticky = ((H & 0x3FFull) | L) != 0ull;
