@@ -150,12 +150,14 @@ def measured_peaks():
 
 
 def source_digest(source: str) -> str:
-    """sha256 over a kernel's own source file and the headers every kernel uses."""
+    """sha256 over a kernel's own source file and every header a kernel can
+    include (csrc/*.cuh, *.h, *.inc and include/*): a change to any of them
+    voids the kernel's recorded DRAM traffic."""
+    import glob
     h = hashlib.sha256()
-    paths = [os.path.join(CSRC, name) for name in (source, "hash32.cuh", "fill_kernel.cuh", "internal.h",
-                                                     "zig_tables.inc")]
-    paths.append(os.path.join(ROOT, "include", "rng_device.cuh"))
-    for path in paths:
+    headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) +
+                     glob.glob(os.path.join(CSRC, "*.inc")) + glob.glob(os.path.join(ROOT, "include", "*")))
+    for path in [os.path.join(CSRC, source)] + headers:
         with open(path, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
