@@ -106,3 +106,18 @@ def test_debug_hooks_without_gpu(rng):
 def test_python_names_match_c_names(rng):
     for name in declared_symbols():
         assert hasattr(rng, name), name
+
+
+def test_package_fails_loudly_without_its_library(tmp_path):
+    """There is no CPU fallback: a copy of the package without the built
+    library refuses to import, naming the missing file."""
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "dropout_lowbias32_hash32_gb300")
+    dst = tmp_path / "dropout_lowbias32_hash32_gb300"
+    shutil.copytree(src, dst, ignore=shutil.ignore_patterns("_lib", "_build", "__pycache__"))
+    res = subprocess.run([sys.executable, "-c", "import dropout_lowbias32_hash32_gb300"], cwd=tmp_path,
+                         capture_output=True, text=True, env={**os.environ, "PYTHONPATH": str(tmp_path)})
+    assert res.returncode != 0
+    assert "ImportError" in res.stderr and "librng_lowbias32.so" in res.stderr
