@@ -137,7 +137,7 @@ class Oracle:
     """numpy front end over one loaded copy of the oracle library."""
 
     def __init__(self, path: str):
-        self.path = os.path.abspath(path)  # identifies this build (each variant has its own file)
+        self.path = os.path.abspath(path)  # identifies the compiled library (each variant has its own file)
         self.lib = _bind(C.CDLL(path))
 
     # Scalar definitions ------------------------------------------------------
