@@ -325,6 +325,23 @@ def test_resume_from_a_counter(rng, torch, orc, name):
     assert np.array_equal(_bits(np.concatenate(parts)), _bits(whole))
 
 
+@pytest.mark.parametrize("world", [2, 3, 8])
+def test_ranks_counter_ranges_concatenate_to_the_fill(rng, torch, orc, world):
+    """The multi-process split (sharding.py) simulated on one GPU: each rank's
+    slice, filled independently from its own first counter, concatenates in
+    rank order to the single-process fill (no rank waits on another)."""
+    from dropout_lowbias32_hash32_gb300 import sharding
+    n, first = 1000003, U32 - 12345
+    for name in ("u64_below_1000", "normal_f64", "exponential_f64", "u8"):
+        gpu, dtype, _ = fills(rng, torch, orc)[name]
+        whole = _host(gpu(_out(torch, dtype, n, 0), first))
+        parts = []
+        for rank in range(world):
+            off, length = sharding.shard(n, rank, world)
+            parts.append(_host(gpu(_out(torch, dtype, length, 0), sharding.first_counter(first, off))))
+        assert np.array_equal(_bits(np.concatenate(parts)), _bits(whole)), (name, world)
+
+
 def test_normal_f64_streams_share_the_miss_list(rng, torch, orc):
     """Fills on two streams use the same per-device miss list in turn."""
     n = 1 << 20
