@@ -222,14 +222,27 @@ int64_t orc_range_i64(uint32_t seed, uint32_t counter, int64_t low, uint64_t b)
 /* randn [Phobos, section randn, std/random.ph:26]                           */
 /* ------------------------------------------------------------------------ */
 
-/* sqrt(-2 log(1 - uniform(seed, 2c))) * cos(6.283185307179586 uniform(seed,
- * 2c+1)), evaluated in binary64 from the two f32 uniforms and returned
- * unrounded to f32 (the reference value the f32 path is held to). */
+/* sqrt(-2 log(1 - u0)) * cos(6.283185307179586 u1) for the uniforms of the
+ * 32-bit draws d0 and d1 (u = (d & 0x7FFFFF) 2^-23, section uniform),
+ * evaluated in binary64 and returned unrounded to f32 (the reference value
+ * the f32 path is held to). */
+double orc_box_muller(uint32_t d0, uint32_t d1)
+{
+    double u0 = (double)(d0 & 0x7FFFFFu) * 0x1p-23;
+    double u1 = (double)(d1 & 0x7FFFFFu) * 0x1p-23;
+    return sqrt(-2.0 * log(1.0 - u0)) * cos(6.283185307179586 * u1);
+}
+
+/* randn(seed, c): the Box-Muller value of the draws at counters 2c and 2c+1
+ * (their f32 uniforms are the uniforms above, exactly). */
 double orc_randn(uint32_t seed, uint32_t counter)
 {
-    double u0 = (double)orc_uniform_f32(seed, 2u * counter);
-    double u1 = (double)orc_uniform_f32(seed, 2u * counter + 1u);
-    return sqrt(-2.0 * log(1.0 - u0)) * cos(6.283185307179586 * u1);
+    return orc_box_muller(orc_draw32(seed, 2u * counter), orc_draw32(seed, 2u * counter + 1u));
+}
+
+void orc_box_muller_fill(const uint32_t *d0, const uint32_t *d1, size_t n, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = orc_box_muller(d0[i], d1[i]);
 }
 
 /* Paired Box-Muller (both branches of one uniform pair, as the tandem

@@ -244,6 +244,24 @@ def pin_randn_special_angles(orc):
     assert zero.size and np.all(orc.fill_randn(seed, 0, idx=zero) == 0)
 
 
+def pin_box_muller_closed_forms(orc):
+    """The Box-Muller value of a draw pair (section randn on the uniforms of
+    section uniform): u0 = 1/2 gives r = sqrt(2 ln 2), u1 = 0 and 1/2 give +r
+    and -r, u1 = 1/4 gives |z| < 1e-15; u0 = 0 gives 0; only the low 23 bits
+    of each draw count; randn(seed, c) is the pair (draw32(2c), draw32(2c+1))."""
+    r = np.sqrt(2.0 * np.log(2.0))
+    hi = np.uint32(0xFF800000)
+    d0 = np.array([1 << 22, 1 << 22, 1 << 22, 0, (1 << 22) | hi, 0x5A5A5A | hi], dtype=np.uint32)
+    d1 = np.array([0, 1 << 22, 1 << 21, 12345, hi, 0x3C3C3C], dtype=np.uint32)
+    z = orc.box_muller_array(d0, d1)
+    assert abs(z[0] - r) <= 1e-15 * r and abs(z[1] + r) <= 1e-15 * r and abs(z[2]) <= 1e-15 * r
+    assert z[3] == 0 and z[4] == z[0]
+    assert z[5] == orc.box_muller_array([0x5A5A5A], [0x3C3C3C])[0]
+    seed = 99
+    w = orc.fill_u32(seed, 0, 2000)
+    assert np.array_equal(orc.box_muller_array(w[0::2], w[1::2]), orc.fill_randn(seed, 0, 1000))
+
+
 def pin_randn_tail_end(orc):
     """Phobos 'Random numbers', randn: the 2^-23 grid ends the tails near 5.6,
     i.e. |z| <= sqrt(-2 ln 2^-23); the largest radius is reached at u0 = 1 - 2^-23."""
@@ -746,7 +764,7 @@ def pin_slice_invariant(orc):
 ALL_PINS = [
     pin_tile_mean, pin_uniform_grid, pin_hash_bijective, pin_draw64_words, pin_narrow_fills,
     pin_lemire_exhaustive_8bit, pin_lemire_exhaustive_16bit, pin_lemire_wide_words,
-    pin_below_distributions, pin_ranges_wrap, pin_randn_special_angles,
+    pin_below_distributions, pin_ranges_wrap, pin_randn_special_angles, pin_box_muller_closed_forms,
     pin_randn_tail_end, pin_randn_distribution, pin_randn_paired, pin_exponentials,
     pin_neglog_f32_exhaustive, pin_neglog_f32_maps_back, pin_neglog_f32_table, pin_exponential_f32_fill,
     pin_cos2pi_exhaustive, pin_cos2pi_coefficients, pin_randn_precise,
