@@ -5,22 +5,67 @@
 // 2c + 1); one value per counter (the cosine branch).
 //
 // Evaluated by lowbias32::randn (include/rng_device.cuh), in f32 on the
-// instruction budget of an HBM-speed fill: 1 - u0 exact; ln(1 - u0) from the
-// Mercator series below u0 = 2^-5 and the hardware log2 above; the hardware
-// sqrt; cos(2 pi u1) = -cos(2 pi (u1 - 1/2)) so the hardware cosine runs on
-// [-pi, pi) (tandem-sycl "Design", section Normals: the angle shifted by half
-// a turn).  Every value is within 4e-6 (1 + |z|) of the exact z.
+// instruction budget of an HBM-speed fill: 1 - u0 exact; -2 ln(1 - u0) as
+// (1 + u0)^2 - 1 below u0 = 2^-7 and from the hardware log2 above; the
+// hardware sqrt and cosine, the angle 2 pi u1 in one fma.  (tandem-sycl
+// "Design", section Normals, shifts the angle by half a turn for its sincos;
+// GB300's cosine is as accurate over the whole turn, so this one does not.)
+// Every value is within 4e-6 (1 + |z|) of the exact z.
 #include "fill_kernel.cuh"
 #include "hash32.cuh"
 
 namespace rngk {
 namespace {
 
+// A vector's four elements at c0 .. c0 + 3 read the draws at 2c0 .. 2c0 + 7.
+// When c0 is a multiple of 4 (for every vector of a launch or for none:
+// c0 = first + head + 4v), a = 2c0 is a multiple of 8, so the eight counters
+// are a ^ i (i < 8) with one a >> 16, and their first xorshifts are
+// x ^ i, x = a ^ (a >> 16) ^ key: one shift for the vector.  The first
+// multiply of the odd draw follows from the even one's, (x ^ 1) M = x M +
+// (x even ? M : -M), with the same sign for the vector's four pairs.  The
+// host picks the aligned or the general generator for the launch (each is
+// its own kernel); both return randn's values bit for bit (the same integer
+// and IEEE operations).
+template <bool kAligned>
 struct GenNormalF32 {
     using T = float;
     static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
+    static constexpr uint32_t kM1 = 0x7FEB352Du;
     uint32_t key;  // folded hash of the seed
     __device__ T operator()(uint32_t c) const { return lowbias32::randn(lowbias32::Key{key}, c); }
+    __device__ Vec16<float> vec(uint32_t c0) const
+    {
+        namespace d = lowbias32::detail;
+        uint32_t b0[4], b1[4];
+        if constexpr (kAligned) {
+            const uint32_t a = c0 << 1;
+            const uint32_t x = a ^ (a >> 16) ^ key;
+            const uint32_t odd_step = (x & 1u) ? 0u - kM1 : kM1;
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j) {
+                const uint32_t xj = x ^ (2u * j);
+                b0[j] = d::one_plus_uniform_bits(d::hash32_middle(xj * kM1));
+                b1[j] = d::one_plus_uniform_bits(d::hash32_middle(xj * kM1 + odd_step));
+            }
+        } else {
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j) {
+                const uint32_t a = (c0 + j) << 1;
+                const uint32_t x = a ^ (a >> 16) ^ key;
+                b0[j] = d::one_plus_uniform_bits(d::hash32_middle(x * kM1));
+                b1[j] = d::one_plus_uniform_bits(d::hash32_middle((x ^ 1u) * kM1));
+            }
+        }
+        const float2 p = d::box_muller_bits_x2(b0[0], b1[0], b0[1], b1[1]);
+        const float2 q = d::box_muller_bits_x2(b0[2], b1[2], b0[3], b1[3]);
+        Vec16<float> v;
+        v.v[0] = p.x;
+        v.v[1] = p.y;
+        v.v[2] = q.x;
+        v.v[3] = q.y;
+        return v;
+    }
 };
 
 // Paired normals: element c is the cosine branch of pair c >> 1 (even c)
@@ -83,7 +128,9 @@ cudaError_t launch_fill_normal_f32_pairs(uint32_t key, uint32_t first, uint32_t 
 
 cudaError_t launch_fill_normal_f32(uint32_t key, uint32_t first, uint32_t n, float *out, cudaStream_t s)
 {
-    return launch_fill(GenNormalF32{key}, out, first, n, s);
+    // the body's vectors start at counters first + head + 4v
+    if (((first + head_elems<float>(out, n)) & 3u) == 0u) return launch_fill(GenNormalF32<true>{key}, out, first, n, s);
+    return launch_fill(GenNormalF32<false>{key}, out, first, n, s);
 }
 
 }  // namespace rngk

@@ -120,40 +120,153 @@ __device__ __forceinline__ float sin_approx(float x)
     return y;
 }
 
-// The Box-Muller radius sqrt(-2 ln(1 - u0)) from the draw d0 at 2c.
-// 1 - u0 = 2 - (1 + u0), exact, in (0, 1].  For u0 < 2^-5 the Mercator
-// series -(u + u^2/2 + ... + u^5/5) (relative error < 1e-7 where the radius
-// is small and an absolutely accurate log is not enough); above, ln 2 times
-// the hardware log2 (absolute error <= 2^-22 on [1/2, 1]).
-__device__ __forceinline__ float box_muller_radius(uint32_t d0)
+// The last xorshift of hash32 fused with the uniform's mask: for y, hash32
+// before its last xorshift (draw d = y ^ (y >> 16)), the bit pattern of
+// 1 + (d & 0x7FFFFF) 2^-23.  Bits 0..22 of d are those of y ^ (y >> 16)
+// (y >> 16 has no bits above 15), and the funnel shift places 0x3F80, the
+// exponent of 1.0f, above y >> 16: one shift and one three-input logic op.
+__device__ __forceinline__ uint32_t one_plus_uniform_bits(uint32_t y)
 {
-    const float one_plus_u0 = __uint_as_float(0x3F800000u | (d0 & 0x7FFFFFu));
-    const float u0 = one_plus_u0 - 1.0f;
-    const float v = 2.0f - one_plus_u0;
-    float series = __fmaf_rn(u0, 0.4f, 0.5f);      // 2 (1 + u/2 + u^2/3 + u^3/4 + u^4/5)
-    series = __fmaf_rn(u0, series, 0.666666687f);
-    series = __fmaf_rn(u0, series, 1.0f);
-    series = __fmaf_rn(u0, series, 2.0f);
-    const float small = u0 * series;               // -2 ln(1 - u0), u0 < 2^-5
-    const float large = -1.38629436f * lg2_approx(v);  // -2 ln 2 log2(1 - u0)
-    return sqrt_approx((d0 & 0x7C0000u) ? large : small);
+    return (y & 0x7FFFFFu) ^ __funnelshift_r(y, 0x3F80u, 16);
 }
 
-// The angle 2 pi (u1 - 1/2) in [-pi, pi) from the draw d1 at 2c + 1, as
-// (1 + u1) 2 pi - 3 pi in one fused multiply-add (within 5e-7 of the exact
-// angle): cos(2 pi u1) = -cos(angle), sin(2 pi u1) = -sin(angle).
-__device__ __forceinline__ float box_muller_angle(uint32_t d1)
+// hash32 from its first multiply's product p up to its last xorshift.
+__device__ __forceinline__ uint32_t hash32_middle(uint32_t p)
 {
-    return __fmaf_rn(__uint_as_float(0x3F800000u | (d1 & 0x7FFFFFu)), 6.28318530717958647692f,
-                     -9.42477796076937971538f);
+    p ^= p >> 15;
+    return p * 0x846CA68Bu;
+}
+
+constexpr float kTwoPi = 6.28318530717958647692f;
+constexpr float kMinusTwoLn2 = -1.38629436f;
+
+// -2 ln(1 - u0) from b0, the bit pattern of 1 + u0, given large = -2 ln 2
+// log2(1 - u0) by the hardware log2 (1 - u0 = 2 - (1 + u0), exact).  For
+// u0 >= 2^-7 (a grid index with a bit in 16..22) that is the value: the
+// log2's absolute error, below 2^-22 on [1/2, 1], moves a radius of at least
+// 0.125 by at most 1.4e-6.  Below, where a log2 near 1 has too little relative
+// accuracy, (1 + u0)^2 - 1 = 2 u0 + u0^2 in one fma, the series of
+// -2 ln(1 - u0) to second order: relative error below u0^2/3 + 2^-24, a
+// radius error below 1.3e-6.  The fma is predicated on the test, so neither
+// a select nor the second candidate costs an instruction where it is not
+// taken.
+__device__ __forceinline__ float radius_squared(uint32_t b0, float large)
+{
+    float s = large;
+    asm("{\n\t.reg .pred p;\n\t.reg .b32 t;\n\t"
+        "and.b32 t, %2, 0x7F0000;\n\t"
+        "setp.eq.u32 p, t, 0;\n\t"
+        "@p fma.rn.f32 %0, %1, %1, 0fBF800000;\n\t}"
+        : "+f"(s)
+        : "f"(__uint_as_float(b0)), "r"(b0));
+    return s;
+}
+
+// The Box-Muller radius sqrt(-2 ln(1 - u0)) from b0, the bit pattern of 1 + u0.
+__device__ __forceinline__ float box_muller_radius(uint32_t b0)
+{
+    const float large = __fmul_rn(lg2_approx(__fsub_rn(2.0f, __uint_as_float(b0))), kMinusTwoLn2);
+    return sqrt_approx(radius_squared(b0, large));
+}
+
+// The angle 2 pi u1 in [0, 2 pi) from b1, the bit pattern of 1 + u1, as
+// (1 + u1) 2 pi - 2 pi in one fused multiply-add (one rounding).  On this
+// grid the hardware cosine and sine are within 2^-20.8 of the exact values
+// over the whole turn, no worse than on [-pi, pi), so the angle needs no
+// half-turn shift and the product no negation.
+__device__ __forceinline__ float box_muller_angle(uint32_t b1)
+{
+    return __fmaf_rn(__uint_as_float(b1), kTwoPi, -kTwoPi);
+}
+
+// randn from the bit patterns of 1 + u0 and 1 + u1.
+__device__ __forceinline__ float box_muller_bits(uint32_t b0, uint32_t b1)
+{
+    return __fmul_rn(box_muller_radius(b0), cos_approx(box_muller_angle(b1)));
+}
+
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 1000
+// Two binary32 lanes in one 64-bit register; add, sub, mul and fma on .f32x2
+// (sm_100 and later) round each lane like the scalar instruction, so the
+// paired evaluation below returns box_muller_bits' values bit for bit.
+__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f32x2_unpack(unsigned long long v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f32x2_sub(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f32x2_mul(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f32x2_fma(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c)
+{
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+#endif
+
+// box_muller_bits for two elements (a and b), the steps other than the
+// hardware log2, square root and cosine paired in f32x2 lanes where the
+// target has them.
+__device__ __forceinline__ float2 box_muller_bits_x2(uint32_t b0a, uint32_t b1a, uint32_t b0b, uint32_t b1b)
+{
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 1000
+    const unsigned long long f0 = f32x2_pack(__uint_as_float(b0a), __uint_as_float(b0b));
+    const float2 v = f32x2_unpack(f32x2_sub(f32x2_pack(2.0f, 2.0f), f0));
+    const float2 large = f32x2_unpack(f32x2_mul(f32x2_pack(lg2_approx(v.x), lg2_approx(v.y)),
+                                                f32x2_pack(kMinusTwoLn2, kMinusTwoLn2)));
+    const float ra = sqrt_approx(radius_squared(b0a, large.x));
+    const float rb = sqrt_approx(radius_squared(b0b, large.y));
+    const float2 angle = f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(b1a), __uint_as_float(b1b)),
+                                                f32x2_pack(kTwoPi, kTwoPi), f32x2_pack(-kTwoPi, -kTwoPi)));
+    return f32x2_unpack(f32x2_mul(f32x2_pack(ra, rb), f32x2_pack(cos_approx(angle.x), cos_approx(angle.y))));
+#else
+    return make_float2(box_muller_bits(b0a, b1a), box_muller_bits(b0b, b1b));
+#endif
 }
 }  // namespace detail
 
-// randn(seed, c) in f32, within 4e-6 (1 + |z|) of the exact value.
+// The Box-Muller value of the 32-bit draws d0 (at 2c) and d1 (at 2c + 1):
+// what randn gives for a counter whose draws these are.
+__device__ __forceinline__ float randn_of_draws(uint32_t d0, uint32_t d1)
+{
+    return detail::box_muller_bits(0x3F800000u | (d0 & 0x7FFFFFu), 0x3F800000u | (d1 & 0x7FFFFFu));
+}
+
+// randn(seed, c) in f32, within 4e-6 (1 + |z|) of the exact value.  The
+// draw at 2c + 1 starts from the draw at 2c's first xorshift ^ 1.
 __device__ __forceinline__ float randn(Key k, uint32_t c)
 {
-    const Words w = draw64_words(k, c);  // the draws at 2c and 2c + 1
-    return -detail::box_muller_radius(w.hi) * detail::cos_approx(detail::box_muller_angle(w.lo));
+    const uint32_t a = c << 1;
+    const uint32_t x = a ^ (a >> 16) ^ k.folded;
+    return detail::box_muller_bits(detail::one_plus_uniform_bits(detail::hash32_middle(x * 0x7FEB352Du)),
+                                   detail::one_plus_uniform_bits(detail::hash32_middle((x ^ 1u) * 0x7FEB352Du)));
+}
+
+// Both Box-Muller branches of the draws d0 and d1: x = r cos(2 pi u1), the
+// value randn_of_draws gives, and y = r sin(2 pi u1).
+__device__ __forceinline__ float2 randn_pair_of_draws(uint32_t d0, uint32_t d1)
+{
+    const float r = detail::box_muller_radius(0x3F800000u | (d0 & 0x7FFFFFu));
+    const float a = detail::box_muller_angle(0x3F800000u | (d1 & 0x7FFFFFu));
+    return make_float2(__fmul_rn(r, detail::cos_approx(a)), __fmul_rn(r, detail::sin_approx(a)));
 }
 
 // Both Box-Muller branches of pair q (the uniforms at 2q and 2q + 1):
@@ -162,9 +275,7 @@ __device__ __forceinline__ float randn(Key k, uint32_t c)
 __device__ __forceinline__ float2 randn_pair(Key k, uint32_t q)
 {
     const Words w = draw64_words(k, q);
-    const float r = detail::box_muller_radius(w.hi);
-    const float a = detail::box_muller_angle(w.lo);
-    return make_float2(-r * detail::cos_approx(a), -r * detail::sin_approx(a));
+    return randn_pair_of_draws(w.hi, w.lo);
 }
 
 // The element with counter c of the paired normal fill: the cosine branch of

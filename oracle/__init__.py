@@ -53,7 +53,8 @@ _SIGS = {
     "orc_below64": (_u64, [_u32, _u32, _u64]),
     "orc_randn": (_f64, [_u32, _u32]),
     "orc_box_muller": (_f64, [_u32, _u32]),
-    "orc_box_muller_fill": (None, [_p, _p, _sz, _p]),
+    "orc_box_muller_sin": (_f64, [_u32, _u32]),
+    "orc_box_muller_fill": (None, [_p, _p, _sz, _p, _p]),
     "orc_dropout": (_f32, [_f32, _f32, _u32, _u32]),
     "orc_zexp": (_f64, [_f64]),
     "orc_zlog": (_f64, [_f64]),
@@ -241,14 +242,16 @@ class Oracle:
         """binary64 values of the randn definition (not rounded to f32)."""
         return self._fill("orc_fill_randn", np.float64, seed, first, n, idx)
 
-    def box_muller_array(self, d0, d1):
-        """binary64 Box-Muller values of the draw pairs (d0[i], d1[i])."""
+    def box_muller_array(self, d0, d1, sine=False):
+        """binary64 Box-Muller values of the draw pairs (d0[i], d1[i]): the
+        cosine branch, or (cosine, sine) with sine=True."""
         d0 = np.ascontiguousarray(d0, dtype=np.uint32)
         d1 = np.ascontiguousarray(d1, dtype=np.uint32)
         assert d0.shape == d1.shape
         out = np.empty(d0.size, dtype=np.float64)
-        self.lib.orc_box_muller_fill(_ptr(d0), _ptr(d1), d0.size, _ptr(out))
-        return out
+        out_sin = np.empty(d0.size, dtype=np.float64) if sine else None
+        self.lib.orc_box_muller_fill(_ptr(d0), _ptr(d1), d0.size, _ptr(out), _ptr(out_sin))
+        return (out, out_sin) if sine else out
 
     def fill_randn_paired(self, seed, first, n=None, idx=None):
         """binary64 values of the paired Box-Muller definition."""

@@ -240,9 +240,23 @@ double orc_randn(uint32_t seed, uint32_t counter)
     return orc_box_muller(orc_draw32(seed, 2u * counter), orc_draw32(seed, 2u * counter + 1u));
 }
 
-void orc_box_muller_fill(const uint32_t *d0, const uint32_t *d1, size_t n, double *out)
+/* The sine branch of the same pair, sqrt(-2 log(1 - u0)) sin(2 pi u1) (the
+ * second value of a Box-Muller pair [Tandem-D, section Normals]). */
+double orc_box_muller_sin(uint32_t d0, uint32_t d1)
 {
-    for (size_t i = 0; i < n; ++i) out[i] = orc_box_muller(d0[i], d1[i]);
+    double u0 = (double)(d0 & 0x7FFFFFu) * 0x1p-23;
+    double u1 = (double)(d1 & 0x7FFFFFu) * 0x1p-23;
+    return sqrt(-2.0 * log(1.0 - u0)) * sin(6.283185307179586 * u1);
+}
+
+/* out[i] = the cosine branch of (d0[i], d1[i]); out_sin[i], if out_sin is
+ * not NULL, the sine branch. */
+void orc_box_muller_fill(const uint32_t *d0, const uint32_t *d1, size_t n, double *out, double *out_sin)
+{
+    for (size_t i = 0; i < n; ++i) {
+        out[i] = orc_box_muller(d0[i], d1[i]);
+        if (out_sin) out_sin[i] = orc_box_muller_sin(d0[i], d1[i]);
+    }
 }
 
 /* Paired Box-Muller (both branches of one uniform pair, as the tandem

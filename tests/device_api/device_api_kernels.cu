@@ -77,4 +77,24 @@ extern "C" int device_api_cos2pi(const uint32_t *m, float *out, uint32_t n)
     return static_cast<int>(cudaDeviceSynchronize());
 }
 
+// randn of given draw pairs: out[i] = lowbias32::randn_of_draws(d0[i], d1[i]),
+// (pair_x[i], pair_y[i]) = lowbias32::randn_pair_of_draws(d0[i], d1[i]).
+__global__ void box_muller_kernel(const uint32_t *d0, const uint32_t *d1, float *out, float *pair_x, float *pair_y,
+                                  uint32_t n)
+{
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        out[i] = lowbias32::randn_of_draws(d0[i], d1[i]);
+        const float2 p = lowbias32::randn_pair_of_draws(d0[i], d1[i]);
+        pair_x[i] = p.x;
+        pair_y[i] = p.y;
+    }
+}
+
+extern "C" int device_api_box_muller(const uint32_t *d0, const uint32_t *d1, float *out, float *pair_x,
+                                     float *pair_y, uint32_t n)
+{
+    box_muller_kernel<<<1024, 256>>>(d0, d1, out, pair_x, pair_y, n);
+    return static_cast<int>(cudaDeviceSynchronize());
+}
+
 extern "C" uint32_t device_api_host_hash32(uint32_t x) { return lowbias32::hash32(x); }

@@ -248,7 +248,9 @@ def pin_box_muller_closed_forms(orc):
     """The Box-Muller value of a draw pair (section randn on the uniforms of
     section uniform): u0 = 1/2 gives r = sqrt(2 ln 2), u1 = 0 and 1/2 give +r
     and -r, u1 = 1/4 gives |z| < 1e-15; u0 = 0 gives 0; only the low 23 bits
-    of each draw count; randn(seed, c) is the pair (draw32(2c), draw32(2c+1))."""
+    of each draw count; randn(seed, c) is the pair (draw32(2c), draw32(2c+1)).
+    The sine branch at the quarter turns, and as the paired fill's odd
+    elements."""
     r = np.sqrt(2.0 * np.log(2.0))
     hi = np.uint32(0xFF800000)
     d0 = np.array([1 << 22, 1 << 22, 1 << 22, 0, (1 << 22) | hi, 0x5A5A5A | hi], dtype=np.uint32)
@@ -260,6 +262,13 @@ def pin_box_muller_closed_forms(orc):
     seed = 99
     w = orc.fill_u32(seed, 0, 2000)
     assert np.array_equal(orc.box_muller_array(w[0::2], w[1::2]), orc.fill_randn(seed, 0, 1000))
+    # the sine branch: u1 = 1/4 gives +r, u1 = 3/4 gives -r, u1 = 0 gives 0;
+    # it is the odd element of the paired fill
+    _, y = orc.box_muller_array(d0[:3], np.array([1 << 21, 3 << 21, 0], dtype=np.uint32), sine=True)
+    assert abs(y[0] - r) <= 1e-15 * r and abs(y[1] + r) <= 1e-15 * r and y[2] == 0
+    x, y = orc.box_muller_array(w[0::2], w[1::2], sine=True)
+    paired = orc.fill_randn_paired(seed, 0, 2000)
+    assert np.array_equal(x, paired[0::2]) and np.array_equal(y, paired[1::2])
 
 
 def pin_randn_tail_end(orc):

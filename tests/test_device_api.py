@@ -41,6 +41,7 @@ def devlib():
     lib.device_api_draws.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32] + [C.c_void_p] * 6
     lib.device_api_neglog.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32]
     lib.device_api_cos2pi.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32]
+    lib.device_api_box_muller.argtypes = [C.c_void_p] * 5 + [C.c_uint32]
     lib.device_api_dropout_rows.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32, C.c_uint32, C.c_float, C.c_uint32,
                                             C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_float)]
     lib.device_api_host_hash32.argtypes = [C.c_uint32]
@@ -100,6 +101,35 @@ def test_header_cos2pi_on_every_input(devlib, orc):
     out = torch.empty(m.size, dtype=torch.float32, device="cuda")
     assert devlib.device_api_cos2pi(mg.data_ptr(), out.data_ptr(), m.size) == 0
     assert np.array_equal(out.cpu().numpy().view(np.uint32), orc.cos2pi_array(m).view(np.uint32))
+
+
+@pytest.mark.gpu
+def test_header_randn_on_every_u0(devlib, orc):
+    """randn_of_draws and randn_pair_of_draws for all 2^23 grid values of u0,
+    within 4e-6 (1 + |z|) of the oracle's binary64 Box-Muller branches: with
+    u1 = 0 (cos = 1, so z is the radius: the series below u0 = 2^-7 and the
+    hardware log2 above it, unmasked), with every u1 against one large radius,
+    and with seeded random angles and random bits above the 23-bit grid.  The
+    pair's cosine branch is randn_of_draws' value bit for bit."""
+    import torch
+    m = np.arange(1 << 23, dtype=np.uint32)
+    gen = np.random.default_rng(20261202)
+    high = gen.integers(0, 1 << 9, m.size, dtype=np.uint32) << np.uint32(23)
+    cases = {"u1 = 0": (m, np.zeros_like(m)),
+             "u0 = 1 - 2^-23, every u1": (np.full_like(m, 0x7FFFFF), m),
+             "random u1": (m | high, gen.integers(0, 1 << 32, m.size, dtype=np.uint64).astype(np.uint32))}
+    out, px, py = (torch.empty(m.size, dtype=torch.float32, device="cuda") for _ in range(3))
+    for name, (d0, d1) in cases.items():
+        g0 = torch.from_numpy(d0.view(np.int32)).cuda()
+        g1 = torch.from_numpy(d1.view(np.int32)).cuda()
+        assert devlib.device_api_box_muller(g0.data_ptr(), g1.data_ptr(), out.data_ptr(), px.data_ptr(),
+                                            py.data_ptr(), m.size) == 0
+        assert torch.equal(out.view(torch.int32), px.view(torch.int32)), name
+        ref_x, ref_y = orc.box_muller_array(d0, d1, sine=True)
+        for got, ref, branch in ((out, ref_x, "cos"), (py, ref_y, "sin")):
+            err = np.abs(got.cpu().numpy().astype(np.float64) - ref) / (1 + np.abs(ref))
+            print(f"randn of draws, {name}, {branch}: worst |err| / (1 + |z|) = {err.max():.3e}")
+            assert err.max() <= 4e-6, (name, branch, int(np.argmax(err)), float(err.max()))
 
 
 def test_header_hash_on_the_host_matches_the_oracle(devlib, orc):

@@ -16,7 +16,8 @@ CANARY = 0xA5
 GUARD = 4096  # bytes on each side
 SIZES = (0, 1, 3, 17, 2047, 2049, 4095, 4097, 8191, 8193, 16385, 3 * 152 * 8 * 256 * 4 + 13)
 NAMES = ["u32", "u64", "f32", "f64", "u32_below_1000", "u64_below_1000", "i32_range", "i64_range32", "i64_range",
-         "normal_f64", "u8", "u16", "f16", "bool", "exponential_f32", "exponential_f64", "normal_f32_precise"]
+         "normal_f64", "u8", "u16", "f16", "bool", "exponential_f32", "exponential_f64", "normal_f32_precise",
+         "normal_f32", "normal_f32_pairs"]
 
 
 @pytest.fixture(scope="module")
