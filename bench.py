@@ -88,7 +88,7 @@ def fill_specs():
           lambda r, o, f, s: r.rng_fill_i64_range32(2, f, W.LOW, 1000, o, s)),
         F("i64_range", "int64", 8, 0, "fill_kernel<GenI64Range>", "fill_bounded.cu",
           lambda r, o, f, s: r.rng_fill_i64_range(3, f, W.LOW, 1000, o, s)),
-        F("normal_f32", "float32", 4, 0, "fill_kernel<GenNormalF32>", "normal_f32.cu",
+        F("normal_f32", "float32", 4, 0, "fill_kernel<GenNormalF32<true>>", "normal_f32.cu",
           lambda r, o, f, s: r.rng_fill_normal_f32(W.NORMAL_SEED, f, o, s)),
         F("normal_f64", "float64", 8, 0, "zig_table_pass+zig_miss_pass", "normal_f64.cu",
           lambda r, o, f, s: r.rng_fill_normal_f64(W.NORMAL_SEED, f, o, s)),

@@ -20,6 +20,17 @@ NAMES = ["u32", "u64", "f32", "f64", "u32_below_1000", "u64_below_1000", "i32_ra
          "normal_f32", "normal_f32_pairs"]
 
 
+def _gpu_fill(rng, torch, orc, name):
+    """The fill's call and output dtype (the f32 Box-Muller fills are held to a
+    tolerance, so the bit-exact parity table does not list them)."""
+    if name == "normal_f32":
+        return (lambda out, first: rng.rng_fill_normal_f32(7, first, out)), torch.float32
+    if name == "normal_f32_pairs":
+        return (lambda out, first: rng.rng_fill_normal_f32_pairs(7, first, out)), torch.float32
+    gpu, dtype, _ = fills(rng, torch, orc)[name]
+    return gpu, dtype
+
+
 @pytest.fixture(scope="module")
 def torch():
     import torch as t
@@ -36,7 +47,7 @@ def rng(torch):
 
 @pytest.mark.parametrize("name", NAMES)
 def test_fill_writes_only_its_elements(rng, torch, orc, name):
-    gpu, dtype, _ = fills(rng, torch, orc)[name]
+    gpu, dtype = _gpu_fill(rng, torch, orc, name)
     size = torch.empty(0, dtype=dtype).element_size()
     for n in SIZES:
         for offset in range(16 // size):
