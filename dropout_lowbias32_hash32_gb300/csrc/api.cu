@@ -353,7 +353,7 @@ uint64_t rng_debug_launch_count(void) { return g_launches.load(); }
 
 rng_status rng_debug_eval_f64(int which, const double *in, double *out, size_t n, void *stream)
 {
-    if (which < 0 || which > 2) return fail(RNG_EINVAL, "rng_debug_eval_f64: which must be 0, 1 or 2");
+    if (which < 0 || which > 4) return fail(RNG_EINVAL, "rng_debug_eval_f64: which must be 0 .. 4");
     if (rng_status st = check_out(in, n, "in")) return st;
     if (rng_status st = check_out(out, n, "out")) return st;
     t_error[0] = '\0';

@@ -104,6 +104,36 @@ __device__ __forceinline__ double scaled_by_u53(Words w, double half_v)
                     __hiloint2double(static_cast<int>(c_hi), static_cast<int>(c_lo)));
 }
 
+// The same product with no FP64 instruction: RNE((m 2^-53) v) for m = w >> 11
+// and v = 2 half_v, bit for bit what scaled_by_u53 returns.  m is normalised,
+// n = (w with its low 11 bits cleared) << clz(hi) in [2^63, 2^64), and v's
+// significand is moved to the top of a 64-bit word (both have 53 significant
+// bits).  The high 64 bits T of their 128-bit product hold the mantissa
+// (T >> 11, or T >> 10 when T's top bit is clear) and the first 10 or 11
+// discarded bits; r, those bits left-aligned, gives the rounding: below one
+// half (r < 2^31) round down, above it round up.  At exactly one half in T
+// the low 64 bits would decide a tie, and for hi = 0 (m < 2^32) the
+// normalisation needs the low word; both return false (about 7e-4 of draws)
+// and the element takes the miss pass, which recomputes it with the fma.
+// The exponent is v/2's, plus T's top bit, minus the normalising shift.
+__device__ __forceinline__ bool scaled_by_u53_int(Words w, double half_v, uint64_t &bits)
+{
+    const uint32_t v_hi = static_cast<uint32_t>(__double2hiint(half_v));
+    const uint32_t v_lo = static_cast<uint32_t>(__double2loint(half_v));
+    const uint32_t z = __clz(w.hi);
+    const uint32_t m_lo = w.lo & 0xFFFFF800u;
+    const uint64_t n = (static_cast<uint64_t>(__funnelshift_l(m_lo, w.hi, z)) << 32) | (m_lo << z);
+    const uint64_t sig = (static_cast<uint64_t>(__funnelshift_l(v_lo, v_hi, 11) | 0x80000000u) << 32) | (v_lo << 11);
+    const uint64_t T = __umul64hi(n, sig);
+    const uint32_t t_hi = static_cast<uint32_t>(T >> 32), t_lo = static_cast<uint32_t>(T);
+    const uint32_t top = t_hi >> 31;
+    const uint32_t shift = 10u + top;
+    const uint32_t r = t_lo << (22u - top);
+    const uint32_t exponent = ((v_hi >> 20) - 1u + top - z) << 20;  // biased, minus the mantissa's leading 1
+    bits = ((static_cast<uint64_t>((t_hi >> shift) + exponent) << 32) | __funnelshift_r(t_lo, t_hi, shift)) + (r >> 31);
+    return (r != 0x80000000u) & (w.hi != 0u);
+}
+
 struct FastDraw {
     uint64_t bits;  // the signed fast-path value
     bool fast;
@@ -229,15 +259,32 @@ __device__ __forceinline__ void warp_queue_flush(uint32_t *q, uint32_t &qn, uint
     qn = rest;
 }
 
-// Fast path with the layer table in shared memory (this lane's copy).
+// Fast path with the layer table in shared memory (this lane's copy).  The
+// test compares the high words only: x and X[j+1] are non-negative, so a
+// smaller high word means x < X[j+1]; an equal one (about 1e-6 of draws) is
+// sent to the miss pass, whose full test decides it.
 __device__ __forceinline__ FastDraw zig_fast_shared(Words w, const double2 *my_copy)
 {
     const uint32_t j = w.lo & (kLayers - 1u);
     const double2 e = my_copy[j * kTableCopies];
     const uint64_t xb = static_cast<uint64_t>(__double_as_longlong(scaled_by_u53(w, e.x)));
     FastDraw d;
-    d.fast = xb < static_cast<uint64_t>(__double_as_longlong(e.y));
+    d.fast = static_cast<uint32_t>(xb >> 32) < static_cast<uint32_t>(__double2hiint(e.y));
     d.bits = xb | (static_cast<uint64_t>(w.lo & 0x400u) << 53);  // bit 10 -> sign bit
+    d.base = j == 0;
+    return d;
+}
+
+// The same with the integer product; a draw it cannot decide is a miss.
+__device__ __forceinline__ FastDraw zig_fast_shared_int(Words w, const double2 *my_copy)
+{
+    const uint32_t j = w.lo & (kLayers - 1u);
+    const double2 e = my_copy[j * kTableCopies];
+    uint64_t xb;
+    const bool exact = scaled_by_u53_int(w, e.x, xb);
+    FastDraw d;
+    d.fast = exact & (static_cast<uint32_t>(xb >> 32) < static_cast<uint32_t>(__double2hiint(e.y)));
+    d.bits = xb | (static_cast<uint64_t>(w.lo & 0x400u) << 53);
     d.base = j == 0;
     return d;
 }
@@ -266,13 +313,15 @@ zig_table_pass(uint32_t key, uint32_t first, double *__restrict__ out, uint32_t 
     };
     // one 16-byte vector (two elements) per lane; misses are rare (a warp
     // step of 64 elements has one with probability 0.24), so the queue is
-    // touched only when the warp's ballot finds one
-    auto step = [&](uint32_t v, bool valid) {
+    // touched only when the warp's ballot finds one.  With int_b (a constant
+    // at each call) the second element's product is the integer one.
+    auto step = [&](uint32_t v, bool valid, bool int_b) {
         const uint32_t e0 = head + 2u * v;
         FastDraw a{}, b{};
         if (valid) {
             a = zig_fast_shared(draw64_words(key, first + e0), my_copy);
-            b = zig_fast_shared(draw64_words(key, first + e0 + 1u), my_copy);
+            b = int_b ? zig_fast_shared_int(draw64_words(key, first + e0 + 1u), my_copy)
+                      : zig_fast_shared(draw64_words(key, first + e0 + 1u), my_copy);
             const uint4 u = make_uint4(static_cast<uint32_t>(a.bits), static_cast<uint32_t>(a.bits >> 32),
                                        static_cast<uint32_t>(b.bits), static_cast<uint32_t>(b.bits >> 32));
             __stcs(reinterpret_cast<uint4 *>(out + e0), u);
@@ -286,11 +335,21 @@ zig_table_pass(uint32_t key, uint32_t first, double *__restrict__ out, uint32_t 
     };
 
     // warp-uniform stride over 16-byte vectors: each warp stores 512
-    // contiguous bytes per step; whole warps first, then the ragged end
+    // contiguous bytes per step; whole warps four steps at a time, then
+    // whole warps, then the ragged end.  GB300 retires 2 DFMA per SM and
+    // cycle, so one product in eight is the integer one: it moves the FP64
+    // pipe's work onto the ALU and FMA pipes as far as the ALU has room
+    // (one in four gains no more, three in eight is slower).
     const uint32_t stride = gridDim.x * kTableThreads;
     uint32_t vb = blockIdx.x * kTableThreads + (threadIdx.x & ~31u);
-    for (; vb + 32u <= n_vec; vb += stride) step(vb + lane, true);
-    for (; vb < n_vec; vb += stride) step(vb + lane, vb + lane < n_vec);
+    for (; vb + 3u * stride + 32u <= n_vec; vb += 4u * stride) {
+        step(vb + lane, true, true);
+        step(vb + stride + lane, true, false);
+        step(vb + 2u * stride + lane, true, false);
+        step(vb + 3u * stride + lane, true, false);
+    }
+    for (; vb + 32u <= n_vec; vb += stride) step(vb + lane, true, false);
+    for (; vb < n_vec; vb += stride) step(vb + lane, vb + lane < n_vec, false);
     // the peeled head and tail (at most one element each), by warp 0 of block 0
     if (blockIdx.x == 0 && threadIdx.x < 32u) {
         const uint32_t tail0 = head + 2u * n_vec;
@@ -331,31 +390,55 @@ zig_miss_pass(uint32_t key, uint32_t normal_key, uint32_t first, double *__restr
             out[e] = zig_slow(key, normal_key, first + e);
         }
     } else {
-        for (uint32_t e = tid; e < n; e += stride)
-            if (!zig_fast(draw64_words(key, first + e)).fast) out[e] = zig_slow(key, normal_key, first + e);
+        // the list overflowed: every element is written again, since the
+        // table pass leaves a deferred draw's value to this pass
+        for (uint32_t e = tid; e < n; e += stride) {
+            const FastDraw d = zig_fast(draw64_words(key, first + e));
+            out[e] = d.fast ? __longlong_as_double(static_cast<long long>(d.bits)) : zig_slow(key, normal_key, first + e);
+        }
     }
+}
+
+// The fast path's magnitude RNE((m 2^-53) X[j]) of the 64-bit draw w (j = w &
+// 1023, m = w >> 11): by the integer product (NaN where it defers the draw)
+// or by the fma.
+__device__ double zig_candidate(unsigned long long w, bool integer)
+{
+    const Words words{static_cast<uint32_t>(w >> 32), static_cast<uint32_t>(w)};
+    const double2 e = __ldg(&kZigHalfXNext[words.lo & (kLayers - 1u)]);
+    if (!integer) return scaled_by_u53(words, e.x);
+    uint64_t bits;
+    return scaled_by_u53_int(words, e.x, bits) ? __longlong_as_double(static_cast<long long>(bits))
+                                               : __longlong_as_double(0x7FF8000000000000ll);
 }
 
 __global__ void eval_f64_kernel(int which, const double *in, double *out, uint32_t n)
 {
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-        out[i] = which == 2 ? neglog64(static_cast<unsigned long long>(__double_as_longlong(in[i])) &
-                                      0x1FFFFFFFFFFFFFull)
-                 : which ? zlog(in[i]) : zexp(in[i]);
+    {
+        const unsigned long long bits = static_cast<unsigned long long>(__double_as_longlong(in[i]));
+        out[i] = which == 4   ? zig_candidate(bits, false)
+                 : which == 3 ? zig_candidate(bits, true)
+                 : which == 2 ? neglog64(bits & 0x1FFFFFFFFFFFFFull)
+                 : which      ? zlog(in[i])
+                              : zexp(in[i]);
+    }
 }
 
-// Expected misses of n elements (p = 0.42766 %, of which the base layer's
-// 5.36e-5) plus 16 standard deviations and slack.
+// Expected entries of n elements plus 16 standard deviations and slack: the
+// misses (p = 0.42766 %, of which the base layer's 5.36e-5) and the draws the
+// integer product defers (one element in eight, about 7.3e-4 of those: at
+// most 1e-4 of elements, in their layer's list).
 size_t wedge_capacity(uint32_t n)
 {
-    const double mean = static_cast<double>(n) * 0.0042766;
+    const double mean = static_cast<double>(n) * (0.0042766 + 1e-4);
     return static_cast<size_t>(mean + 16.0 * std::sqrt(mean + 1.0) + 4096.0);
 }
 
 size_t tail_capacity(uint32_t n)
 {
-    const double mean = static_cast<double>(n) * 5.36e-5;
+    const double mean = static_cast<double>(n) * (5.36e-5 + 1e-7);
     return static_cast<size_t>(mean + 16.0 * std::sqrt(mean + 1.0) + 1024.0);
 }
 

@@ -250,9 +250,12 @@ const char *rng_last_error(void);
  * device. */
 rng_status rng_debug_set_miss_capacity(size_t capacity);
 
-/* Number of misses the most recent normal_f64 fill's table pass recorded on
+/* Number of entries the most recent normal_f64 fill's table pass listed on
  * the current device (of its last chunk of at most 2^31 elements; above the
- * capacity when the list overflowed).  Synchronises the device. */
+ * capacity when the list overflowed): every draw that misses the fast path,
+ * plus the few fast draws the table pass leaves to the second kernel (those
+ * its integer product cannot round, about 1e-4 of the elements, and about
+ * 1e-6 whose product shares X[j+1]'s high word).  Synchronises the device. */
 rng_status rng_debug_last_miss_count(uint64_t *count);
 
 /* Number of kernels this library has launched since it was loaded, over all
@@ -263,7 +266,11 @@ uint64_t rng_debug_launch_count(void);
  * f(in[i]) for i < n (in and out device arrays of doubles): the normal_f64
  * slow path's exp (which = 0) or log (which = 1), or (which = 2) the f64
  * exponential's fixed-point -ln(1 - m 2^-53) with m the low 53 bits of
- * in[i]'s bit pattern.  For checking those functions on chosen inputs. */
+ * in[i]'s bit pattern.  which = 3 and 4 take in[i]'s bit pattern as a 64-bit
+ * ziggurat draw w and return its fast-path magnitude RNE((w >> 11) 2^-53
+ * X[w & 1023]): by the table pass's integer product (NaN for a draw it
+ * defers to the miss pass) and by its fma.  For checking those functions on
+ * chosen inputs; which outside 0 .. 4 is RNG_EINVAL. */
 rng_status rng_debug_eval_f64(int which, const double *in, double *out, size_t n, void *stream);
 
 /* A measurement aid with no counterpart on the pages: the write ceiling the

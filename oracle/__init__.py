@@ -61,6 +61,7 @@ _SIGS = {
     "orc_zig_table": (C.c_int, [C.c_uint, _p, _p, C.POINTER(_f64), C.POINTER(_f64)]),
     "orc_zig1024": (None, [_p, _p]),
     "orc_zig_first_draw_fast": (C.c_int, [_u32, _u32]),
+    "orc_zig_candidates": (None, [_p, _sz, _p]),
     "orc_normal_f64": (_f64, [_u32, _u32]),
     "orc_fill_u32": (None, [_u32, _u32, _sz, _p, _p]),
     "orc_fill_u64": (None, [_u32, _u32, _sz, _p, _p]),
@@ -184,6 +185,14 @@ class Oracle:
         if self.lib.orc_zig_table(N, _ptr(X), _ptr(F), C.byref(r), C.byref(v)) != 0:
             raise ValueError("N must be at least 2")
         return X, F, r.value, v.value
+
+    def zig_candidates(self, w):
+        """The ziggurat fast path's magnitude RNE((w >> 11) 2^-53 X[w & 1023])
+        of each 64-bit draw w, fast or not."""
+        w = np.ascontiguousarray(w, dtype=np.uint64)
+        x = np.empty(w.size, dtype=np.float64)
+        self.lib.orc_zig_candidates(_ptr(w), w.size, _ptr(x))
+        return x
 
     def zig1024(self):
         X = np.empty(1025, np.float64)

@@ -771,6 +771,16 @@ static int zig_fast(uint64_t w, double *x_out, unsigned *j_out, int *neg_out)
     return x < zig_X[j + 1];
 }
 
+/* x[i] = the fast path's magnitude (w[i] >> 11) 2^-53 X[j] (one rounded
+ * multiply, j = w[i] & 1023) of each 64-bit draw, fast or not. */
+void orc_zig_candidates(const uint64_t *w, size_t n, double *x)
+{
+    unsigned j;
+    int neg;
+    zig_init();
+    for (size_t i = 0; i < n; ++i) zig_fast(w[i], &x[i], &j, &neg);
+}
+
 /* 1 when the element's first draw takes the fast path, 0 when it misses. */
 int orc_zig_first_draw_fast(uint32_t seed, uint32_t counter)
 {

@@ -664,6 +664,23 @@ def pin_zig_table_invariants(orc):
     assert abs((r * F[1] + tail) / v - 1) < 1e-14
 
 
+def pin_zig_candidate_rounding(orc):
+    """The fast path's magnitude is the correctly rounded product of the
+    53-bit draw and X[j] (Fraction -> float rounds to nearest even): random
+    draws over every layer, draws with many leading zeros, and m = 2^53 - 1."""
+    from fractions import Fraction
+    X, _ = orc.zig1024()
+    gen = np.random.default_rng(5)
+    w = gen.integers(0, 1 << 63, 4000, dtype=np.uint64) * np.uint64(2) + gen.integers(0, 2, 4000, dtype=np.uint64)
+    w[:1024] = (w[:1024] & ~np.uint64(1023)) | np.arange(1024, dtype=np.uint64)
+    w[1024:1088] >>= np.arange(64, dtype=np.uint64)
+    w[1088] = np.uint64((1 << 64) - 1)
+    x = orc.zig_candidates(w)
+    for wi, xi in zip(w.tolist(), x.tolist()):
+        exact = Fraction(wi >> 11, 1 << 53) * Fraction(float(X[wi & 1023]))
+        assert xi == float(exact), (hex(wi), xi, float(exact))
+
+
 def pin_zig_miss_rate(orc):
     """tandem-sycl 'Design', Normals: 0.43 % of draws miss the fast path.  The
     table's miss probability mean(1 - X[j+1]/X[j]) rounds to it, and the
@@ -779,6 +796,6 @@ ALL_PINS = [
     pin_cos2pi_exhaustive, pin_cos2pi_coefficients, pin_randn_precise,
     pin_neglog64_accuracy, pin_neglog64_table, pin_exponential_f64_fill,
     pin_dropout, pin_zexp_zlog,
-    pin_zig_table_published, pin_zig_table_invariants, pin_zig_miss_rate,
+    pin_zig_table_published, pin_zig_table_invariants, pin_zig_candidate_rounding, pin_zig_miss_rate,
     pin_normal_f64_distribution, pin_zig_wedge_acceptance, pin_slice_invariant,
 ]

@@ -91,7 +91,8 @@ def test_dropout_partial_overlap_rejected(rng):
 
 
 def test_debug_hooks_without_gpu(rng):
-    assert rng.raw("rng_debug_eval_f64")(3, None, None, 0, None) == rng.RNG_EINVAL
+    assert rng.raw("rng_debug_eval_f64")(5, None, None, 0, None) == rng.RNG_EINVAL
+    assert rng.raw("rng_debug_eval_f64")(-1, None, None, 0, None) == rng.RNG_EINVAL
     assert rng.raw("rng_debug_last_miss_count")(None) == rng.RNG_EINVAL
     assert rng.rng_debug_launch_count() >= 0
     rng.rng_debug_set_miss_capacity(None)

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 from dropout_lowbias32_hash32_gb300 import workloads as W
+from test_gpu_parity import deferred_bounds
 
 pytestmark = pytest.mark.gpu
 
@@ -105,7 +106,8 @@ def test_full_size_sampled(rng, torch, orc, sample, name, dtype, gpu, ref):
 
 def test_full_size_normal_f64_every_miss(rng, torch, orc):
     """Every element whose first draw misses (about 1.15 million at 2^28) is
-    compared, and the miss count matches the oracle's fast-path test."""
+    compared, and the list holds the oracle's misses and the few fast draws
+    the table pass defers."""
     out = torch.empty(N, dtype=torch.float64, device="cuda")
     rng.rng_fill_normal_f64(W.NORMAL_SEED, 1, out)
     torch.cuda.synchronize()
@@ -115,9 +117,10 @@ def test_full_size_normal_f64_every_miss(rng, torch, orc):
     for a in range(0, N, step):
         fast[a:a + step] = orc.fill_zig_fast(W.NORMAL_SEED, 1 + a, step)
     miss_idx = np.nonzero(fast == 0)[0]
-    assert misses == miss_idx.size
+    lo, hi = deferred_bounds(N)
+    assert lo < misses - miss_idx.size < hi, (misses, miss_idx.size)
     p = 0.0042766
-    assert abs(misses - p * N) < 5 * math.sqrt(p * N)
+    assert abs(miss_idx.size - p * N) < 5 * math.sqrt(p * N)
     _eq("normal_f64 misses", _gather(torch, out, miss_idx), orc.fill_normal_f64(W.NORMAL_SEED, 1, idx=miss_idx))
     del out
     torch.cuda.empty_cache()
