@@ -167,21 +167,42 @@ __device__ __forceinline__ double u53_open(Words w)
 // substream key, folded: its 64-bit word k is draw64_words(skf, k).
 // The wedge test y < zexp(-x^2/2) decided in binary32 where that is safe: +1
 // (accept) or -1 (reject) when y lies outside exp(-x^2/2) (1 -+ 2^-16),
-// else 0 (take the exact test).  The binary32 estimate is within 2^-18 of
-// exp(-x^2/2) (the roundings of x, y and -x^2/2, at most 2^-22 of
-// |x^2/2| <= 8.2, and __expf's documented 2 + 1.173 |t| ulp), and zexp is
+// else 0 (take the exact test).  x and y enter as binary32 truncations of
+// their bits (relative error below 2^-23 each: GB300 converts binary64 on its
+// narrow FP64 pipe), so -x^2/2 carries at most 3 2^-23 + 2^-24 of |x^2/2| <=
+// 8.2 and __expf its documented 2 + 1.173 |t| ulp: with y's truncation and
+// the margin's product the estimate is within 5e-6 (2^-17.6) of the exact
+// comparison, inside the margin of 1.5e-5 (2^-16).  zexp is
 // within 2 ulp of binary64 exp, so a screened decision is the exact one and
 // the values stay those of the exact test.  Candidates inside the margin
-// (about one in 10^3) take the binary64 path; the screen saves the 18 FP64
-// operations of zexp on the rest.
+// (about one in 10^3) take the binary64 path.
+__device__ __forceinline__ float float_rz_of_positive(double d)
+{
+    // a normal binary64 in binary32's range, truncated: the 11-bit exponent
+    // and the top 23 mantissa bits sit in bits 23..33 and 0..22 of the word
+    // shifted right by 29; rebias the exponent by 1023 - 127 modulo 2^32
+    const uint32_t w = __funnelshift_r(static_cast<uint32_t>(__double2loint(d)),
+                                       static_cast<uint32_t>(__double2hiint(d)), 29);
+    return __uint_as_float(w - (896u << 23));
+}
+
 __device__ __forceinline__ int wedge_screen(double x, double y)
 {
-    const float x32 = __double2float_rn(x);
+    const float x32 = float_rz_of_positive(x);
     const float e32 = __expf(__fmul_rn(__fmul_rn(x32, x32), -0.5f));
-    const float y32 = __double2float_rn(y);
+    const float y32 = float_rz_of_positive(y);
     if (y32 < __fmul_rn(e32, 1.0f - 0x1p-16f)) return 1;
     if (y32 > __fmul_rn(e32, 1.0f + 0x1p-16f)) return -1;
     return 0;
+}
+
+// The fast path's product of draw w with v = 2 half_v, by the integer form
+// where it decides and the fma where it defers.
+__device__ __forceinline__ double scaled_by_u53_any(Words w, double half_v)
+{
+    uint64_t bits;
+    if (scaled_by_u53_int(w, half_v, bits)) return __longlong_as_double(static_cast<long long>(bits));
+    return scaled_by_u53(w, half_v);
 }
 
 __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint32_t c)
@@ -193,7 +214,7 @@ __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint3
         const uint32_t j = w.lo & (kLayers - 1u);
         const bool neg = w.lo & 0x400u;
         const double2 e = __ldg(&kZigHalfXNext[j]);
-        const double x = scaled_by_u53(w, e.x);
+        const double x = scaled_by_u53_any(w, e.x);
         if (__double_as_longlong(x) < __double_as_longlong(e.y)) return neg ? -x : x;
         if (j == 0) {
             const double r = kZigX[1];
