@@ -112,6 +112,22 @@ struct GenNormalF32Precise {
     static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     uint32_t key;
     __device__ T operator()(uint32_t c) const { return lowbias32::randn_precise(lowbias32::Key{key}, c); }
+    // a vector's four values, the float steps two at a time
+    // (lowbias32::detail::randn_precise_x2: the same values)
+    __device__ Vec16<float> vec(uint32_t c0) const
+    {
+        const lowbias32::Key k{key};
+        const lowbias32::Words w0 = lowbias32::draw64_words(k, c0), w1 = lowbias32::draw64_words(k, c0 + 1u);
+        const lowbias32::Words w2 = lowbias32::draw64_words(k, c0 + 2u), w3 = lowbias32::draw64_words(k, c0 + 3u);
+        const float2 a = lowbias32::detail::randn_precise_x2(w0.hi, w0.lo, w1.hi, w1.lo);
+        const float2 b = lowbias32::detail::randn_precise_x2(w2.hi, w2.lo, w3.hi, w3.lo);
+        Vec16<float> v;
+        v.v[0] = a.x;
+        v.v[1] = a.y;
+        v.v[2] = b.x;
+        v.v[3] = b.y;
+        return v;
+    }
 };
 
 }  // namespace

@@ -188,7 +188,9 @@ __device__ __forceinline__ float box_muller_bits(uint32_t b0, uint32_t b1)
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 1000
 // Two binary32 lanes in one 64-bit register; add, sub, mul and fma on .f32x2
 // (sm_100 and later) round each lane like the scalar instruction, so the
-// paired evaluation below returns box_muller_bits' values bit for bit.
+// paired evaluation below returns box_muller_bits' values bit for bit.  A
+// paired multiply whose result feeds a paired add may be contracted into one
+// fma, unlike a scalar __fmul_rn: paired code here keeps such products scalar.
 __device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi)
 {
     unsigned long long r;
@@ -205,6 +207,12 @@ __device__ __forceinline__ unsigned long long f32x2_sub(unsigned long long a, un
 {
     unsigned long long d;
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f32x2_add(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 __device__ __forceinline__ unsigned long long f32x2_mul(unsigned long long a, unsigned long long b)
@@ -337,6 +345,46 @@ __device__ __forceinline__ float neg_log_grid(uint32_t m)
 // -ln(1 - u) for u = uniform(k, c), by neg_log_grid; in [0, 23 ln 2].
 __device__ __forceinline__ float exponential(Key k, uint32_t c) { return neg_log_grid(draw32(k, c) & 0x7FFFFFu); }
 
+namespace detail {
+// neg_log_grid of two inputs, its float steps paired in f32x2 lanes where the
+// target has them (each lane rounded like the scalar step, so the values are
+// neg_log_grid's bit for bit).  -r - bb is formed as -(r + bb), the same
+// value with the same sign of zero, since RN is symmetric.
+__device__ __forceinline__ float2 neg_log_grid_x2(uint32_t ma, uint32_t mb)
+{
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 1000
+    const float2 V = f32x2_unpack(f32x2_sub(f32x2_pack(__uint_as_float(0x4B000000u | (0x800000u - ma)),
+                                                       __uint_as_float(0x4B000000u | (0x800000u - mb))),
+                                            f32x2_pack(8388608.0f, 8388608.0f)));
+    const uint32_t bits_a = __float_as_uint(V.x), bits_b = __float_as_uint(V.y);
+    const uint32_t mant_a = bits_a & 0x7FFFFFu, mant_b = bits_b & 0x7FFFFFu;
+    const float4 ta = __ldg(&kNegLogTable[(mant_a + 16384u) >> 15]);
+    const float4 tb = __ldg(&kNegLogTable[(mant_b + 16384u) >> 15]);
+    const unsigned long long M = f32x2_pack(__uint_as_float(mant_a | 0x3F800000u), __uint_as_float(mant_b | 0x3F800000u));
+    const unsigned long long E = f32x2_sub(f32x2_pack(__uint_as_float(0x4B000000u | (150u - (bits_a >> 23))),
+                                                      __uint_as_float(0x4B000000u | (150u - (bits_b >> 23)))),
+                                           f32x2_pack(8388608.0f, 8388608.0f));
+    const unsigned long long r = f32x2_fma(M, f32x2_pack(ta.x, tb.x), f32x2_pack(-1.0f, -1.0f));
+    const unsigned long long t_hi = f32x2_fma(E, f32x2_pack(kNegLogLn2Hi, kNegLogLn2Hi), f32x2_pack(ta.y, tb.y));
+    const unsigned long long t_lo = f32x2_fma(E, f32x2_pack(kNegLogLn2Lo, kNegLogLn2Lo), f32x2_pack(ta.z, tb.z));
+    const unsigned long long s = f32x2_sub(t_hi, r);
+    const unsigned long long bb = f32x2_sub(s, t_hi);
+    const unsigned long long err = f32x2_sub(f32x2_sub(t_hi, f32x2_sub(s, bb)), f32x2_add(r, bb));
+    unsigned long long p = f32x2_fma(r, f32x2_pack(-0x1.99999ap-3f, -0x1.99999ap-3f), f32x2_pack(0.25f, 0.25f));
+    p = f32x2_fma(r, p, f32x2_pack(-0x1.555556p-2f, -0x1.555556p-2f));
+    p = f32x2_fma(r, p, f32x2_pack(0.5f, 0.5f));
+    // the tail's last product is rounded on its own before the sum: in
+    // scalar steps, which are never fused into the add that follows (a paired
+    // multiply feeding a paired add was seen contracted into one fma)
+    const float2 rr = f32x2_unpack(f32x2_mul(r, r)), pf = f32x2_unpack(p);
+    const unsigned long long tail = f32x2_pack(__fmul_rn(rr.x, pf.x), __fmul_rn(rr.y, pf.y));
+    return f32x2_unpack(f32x2_add(s, f32x2_add(f32x2_add(err, t_lo), tail)));
+#else
+    return make_float2(neg_log_grid(ma), neg_log_grid(mb));
+#endif
+}
+}  // namespace detail
+
 // ---- precise normal --------------------------------------------------------------
 
 namespace detail {
@@ -371,6 +419,41 @@ __device__ __forceinline__ float cos2pi_grid(uint32_t m)
     return (q == 1u || q == 2u) ? -v : v;
 }
 
+namespace detail {
+// cos2pi_grid of two inputs, its float steps paired in f32x2 lanes where the
+// target has them (the values are cos2pi_grid's bit for bit).
+__device__ __forceinline__ float2 cos2pi_grid_x2(uint32_t ma, uint32_t mb)
+{
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 1000
+    const uint32_t qa = ma >> 21, qb = mb >> 21;
+    const uint32_t fa = ma & 0x1FFFFFu, fb = mb & 0x1FFFFFu;
+    const bool swap_a = fa > 0x100000u, swap_b = fb > 0x100000u;
+    const unsigned long long g = f32x2_sub(
+        f32x2_pack(__uint_as_float(0x4B000000u | (swap_a ? 0x200000u - fa : fa)),
+                   __uint_as_float(0x4B000000u | (swap_b ? 0x200000u - fb : fb))),
+        f32x2_pack(8388608.0f, 8388608.0f));
+    const unsigned long long x = f32x2_mul(g, f32x2_pack(0x1p-23f, 0x1p-23f));
+    const unsigned long long x2 = f32x2_mul(x, x);
+    unsigned long long p = f32x2_fma(x2, f32x2_pack(kCos2PiS9, kCos2PiS9), f32x2_pack(kCos2PiS7, kCos2PiS7));
+    p = f32x2_fma(x2, p, f32x2_pack(kCos2PiS5, kCos2PiS5));
+    p = f32x2_fma(x2, p, f32x2_pack(kCos2PiS3, kCos2PiS3));
+    p = f32x2_fma(x2, p, f32x2_pack(kCos2PiS1Lo, kCos2PiS1Lo));
+    const float2 sin_x = f32x2_unpack(f32x2_fma(x, f32x2_pack(kCos2PiS1Hi, kCos2PiS1Hi), f32x2_mul(x, p)));
+    unsigned long long c = f32x2_fma(x2, f32x2_pack(kCos2PiC10, kCos2PiC10), f32x2_pack(kCos2PiC8, kCos2PiC8));
+    c = f32x2_fma(x2, c, f32x2_pack(kCos2PiC6, kCos2PiC6));
+    c = f32x2_fma(x2, c, f32x2_pack(kCos2PiC4, kCos2PiC4));
+    const unsigned long long t = f32x2_mul(x2, f32x2_fma(x2, c, f32x2_pack(kCos2PiC2Lo, kCos2PiC2Lo)));
+    const float2 cos_x = f32x2_unpack(f32x2_add(f32x2_pack(1.0f, 1.0f),
+                                                f32x2_fma(x2, f32x2_pack(kCos2PiC2Hi, kCos2PiC2Hi), t)));
+    const float va = ((qa & 1u) != 0u) != swap_a ? sin_x.x : cos_x.x;
+    const float vb = ((qb & 1u) != 0u) != swap_b ? sin_x.y : cos_x.y;
+    return make_float2((qa == 1u || qa == 2u) ? -va : va, (qb == 1u || qb == 2u) ? -vb : vb);
+#else
+    return make_float2(cos2pi_grid(ma), cos2pi_grid(mb));
+#endif
+}
+}  // namespace detail
+
 // randn's definition (the uniforms at 2c and 2c + 1, cosine branch) evaluated
 // in binary32 to a few ulp: sqrt(2 neg_log_grid(u0)) cos2pi_grid(u1) with an
 // IEEE square root; within 2.5 ulp of the exact value (tandem-sycl "Design",
@@ -382,6 +465,24 @@ __device__ __forceinline__ float randn_precise(Key k, uint32_t c)
     const float e = neg_log_grid(w.hi & 0x7FFFFFu);
     return __fmul_rn(__fsqrt_rn(__fadd_rn(e, e)), cos2pi_grid(w.lo & 0x7FFFFFu));
 }
+
+namespace detail {
+// randn_precise of the draw pairs (a0, a1) and (b0, b1), the float steps
+// paired in f32x2 lanes where the target has them (same values).
+__device__ __forceinline__ float2 randn_precise_x2(uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1)
+{
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 1000
+    const float2 e = neg_log_grid_x2(a0 & 0x7FFFFFu, b0 & 0x7FFFFFu);
+    const float2 c = cos2pi_grid_x2(a1 & 0x7FFFFFu, b1 & 0x7FFFFFu);
+    const float2 twice = f32x2_unpack(f32x2_add(f32x2_pack(e.x, e.y), f32x2_pack(e.x, e.y)));
+    return f32x2_unpack(f32x2_mul(f32x2_pack(__fsqrt_rn(twice.x), __fsqrt_rn(twice.y)), f32x2_pack(c.x, c.y)));
+#else
+    const float ea = neg_log_grid(a0 & 0x7FFFFFu), eb = neg_log_grid(b0 & 0x7FFFFFu);
+    return make_float2(__fmul_rn(__fsqrt_rn(__fadd_rn(ea, ea)), cos2pi_grid(a1 & 0x7FFFFFu)),
+                       __fmul_rn(__fsqrt_rn(__fadd_rn(eb, eb)), cos2pi_grid(b1 & 0x7FFFFFu)));
+#endif
+}
+}  // namespace detail
 
 // ---- dropout ------------------------------------------------------------------
 

@@ -52,28 +52,51 @@ extern "C" int device_api_dropout_rows(const float *x, float *y, uint32_t rows, 
 
 // The header's own f32 logarithm on given 23-bit inputs: out[i] =
 // -ln(1 - m[i] 2^-23) by lowbias32::neg_log_grid.
-__global__ void neglog_kernel(const uint32_t *m, float *out, uint32_t n)
+// With paired = 1, elements 2q and 2q + 1 go through the paired form
+// (detail::neg_log_grid_x2, the fills' form); n must then be even.
+__global__ void neglog_kernel(const uint32_t *m, float *out, uint32_t n, int paired)
 {
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    const uint32_t stride = gridDim.x * blockDim.x;
+    if (paired) {
+        for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < n / 2u; q += stride) {
+            const float2 v = lowbias32::detail::neg_log_grid_x2(m[2u * q] & 0x7FFFFFu, m[2u * q + 1u] & 0x7FFFFFu);
+            out[2u * q] = v.x;
+            out[2u * q + 1u] = v.y;
+        }
+        return;
+    }
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
         out[i] = lowbias32::neg_log_grid(m[i] & 0x7FFFFFu);
 }
 
-extern "C" int device_api_neglog(const uint32_t *m, float *out, uint32_t n)
+extern "C" int device_api_neglog(const uint32_t *m, float *out, uint32_t n, int paired)
 {
-    neglog_kernel<<<1024, 256>>>(m, out, n);
+    if (paired && (n & 1u)) return -1;
+    neglog_kernel<<<1024, 256>>>(m, out, n, paired);
     return static_cast<int>(cudaDeviceSynchronize());
 }
 
 // The header's own cos(2 pi m 2^-23) on given 23-bit inputs (cos2pi_grid).
-__global__ void cos2pi_kernel(const uint32_t *m, float *out, uint32_t n)
+// With paired = 1, elements 2q and 2q + 1 go through detail::cos2pi_grid_x2.
+__global__ void cos2pi_kernel(const uint32_t *m, float *out, uint32_t n, int paired)
 {
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    const uint32_t stride = gridDim.x * blockDim.x;
+    if (paired) {
+        for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < n / 2u; q += stride) {
+            const float2 v = lowbias32::detail::cos2pi_grid_x2(m[2u * q] & 0x7FFFFFu, m[2u * q + 1u] & 0x7FFFFFu);
+            out[2u * q] = v.x;
+            out[2u * q + 1u] = v.y;
+        }
+        return;
+    }
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
         out[i] = lowbias32::cos2pi_grid(m[i] & 0x7FFFFFu);
 }
 
-extern "C" int device_api_cos2pi(const uint32_t *m, float *out, uint32_t n)
+extern "C" int device_api_cos2pi(const uint32_t *m, float *out, uint32_t n, int paired)
 {
-    cos2pi_kernel<<<1024, 256>>>(m, out, n);
+    if (paired && (n & 1u)) return -1;
+    cos2pi_kernel<<<1024, 256>>>(m, out, n, paired);
     return static_cast<int>(cudaDeviceSynchronize());
 }
 

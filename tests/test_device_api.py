@@ -39,8 +39,8 @@ def devlib():
         os.replace(so + ".tmp", so)
     lib = C.CDLL(so)
     lib.device_api_draws.argtypes = [C.c_uint32, C.c_uint32, C.c_uint32] + [C.c_void_p] * 6
-    lib.device_api_neglog.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32]
-    lib.device_api_cos2pi.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32]
+    lib.device_api_neglog.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32, C.c_int]
+    lib.device_api_cos2pi.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32, C.c_int]
     lib.device_api_box_muller.argtypes = [C.c_void_p] * 5 + [C.c_uint32]
     lib.device_api_dropout_rows.argtypes = [C.c_void_p, C.c_void_p, C.c_uint32, C.c_uint32, C.c_float, C.c_uint32,
                                             C.c_int, C.POINTER(C.c_int), C.POINTER(C.c_float)]
@@ -72,13 +72,20 @@ def test_header_neglog_table_matches_the_oracle(orc):
 
 @pytest.mark.gpu
 def test_header_neglog_on_every_input(devlib, orc):
-    """neg_log_grid on all 2^23 inputs equals the oracle's own f32 log, bit for bit."""
+    """neg_log_grid on all 2^23 inputs equals the oracle's own f32 log, bit for
+    bit, alone and in the paired f32x2 form the fills use (each input paired
+    with its neighbour and, reversed, with another)."""
     import torch
     m = np.arange(1 << 23, dtype=np.uint32)
-    mg = torch.from_numpy(m.view(np.int32)).cuda()
+    want = orc.neglog_array(m).view(np.uint32)
     out = torch.empty(m.size, dtype=torch.float32, device="cuda")
-    assert devlib.device_api_neglog(mg.data_ptr(), out.data_ptr(), m.size) == 0
-    assert np.array_equal(out.cpu().numpy().view(np.uint32), orc.neglog_array(m).view(np.uint32))
+    for order, paired in ((m, 0), (m, 1), (m[::-1].copy(), 1)):
+        mg = torch.from_numpy(order.view(np.int32)).cuda()
+        assert devlib.device_api_neglog(mg.data_ptr(), out.data_ptr(), m.size, paired) == 0
+        got = out.cpu().numpy().view(np.uint32)
+        bad = np.nonzero(got != want[order])[0]
+        assert bad.size == 0, (paired, bad.size, [(int(i), int(order[i]), hex(int(got[i])), hex(int(want[order][i])))
+                                                  for i in bad[:8]])
 
 
 def test_header_cos2pi_coefficients_match_the_oracle(orc):
@@ -94,13 +101,19 @@ def test_header_cos2pi_coefficients_match_the_oracle(orc):
 
 @pytest.mark.gpu
 def test_header_cos2pi_on_every_input(devlib, orc):
-    """cos2pi_grid on all 2^23 inputs equals the oracle's own cosine, bit for bit."""
+    """cos2pi_grid on all 2^23 inputs equals the oracle's own cosine, bit for
+    bit, alone and in the paired f32x2 form the precise fill uses."""
     import torch
     m = np.arange(1 << 23, dtype=np.uint32)
-    mg = torch.from_numpy(m.view(np.int32)).cuda()
+    want = orc.cos2pi_array(m).view(np.uint32)
     out = torch.empty(m.size, dtype=torch.float32, device="cuda")
-    assert devlib.device_api_cos2pi(mg.data_ptr(), out.data_ptr(), m.size) == 0
-    assert np.array_equal(out.cpu().numpy().view(np.uint32), orc.cos2pi_array(m).view(np.uint32))
+    for order, paired in ((m, 0), (m, 1), (m[::-1].copy(), 1)):
+        mg = torch.from_numpy(order.view(np.int32)).cuda()
+        assert devlib.device_api_cos2pi(mg.data_ptr(), out.data_ptr(), m.size, paired) == 0
+        got = out.cpu().numpy().view(np.uint32)
+        bad = np.nonzero(got != want[order])[0]
+        assert bad.size == 0, (paired, bad.size, [(int(i), int(order[i]), hex(int(got[i])), hex(int(want[order][i])))
+                                                  for i in bad[:8]])
 
 
 @pytest.mark.gpu
