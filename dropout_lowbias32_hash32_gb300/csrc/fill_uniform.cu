@@ -70,7 +70,7 @@ __device__ __forceinline__ double scaled_u53_to_double(Words w)
 
 struct GenF64 {
     using T = double;
-    static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
+    static constexpr uint32_t kVectorsPerThread = 16;  // measured at 2^28: 1.1 % faster than 8, 2 % than 4
     uint32_t key;
     __device__ T operator()(uint32_t c) const { return scaled_u53_to_double(draw64_words(key, c)); }
     // both elements of a 16-byte vector, one branch on a zero high word

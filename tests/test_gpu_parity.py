@@ -424,6 +424,17 @@ def test_ziggurat_integer_product(rng, torch, orc):
     assert deferred[:1 << 18].mean() < 2e-3  # random draws: about 7.3e-4
 
 
+def test_normal_f64_unrolled_table_pass(rng, torch, orc):
+    """A fill long enough for the table pass's four-step loop (one product in
+    eight by the integer form), with a one-element head (output 8 bytes off a
+    16-byte boundary), a ragged tail and counters that wrap: every element
+    equals the oracle's."""
+    n = (1 << 22) + 5
+    first = U32 - 3
+    out = rng.rng_fill_normal_f64(7, first, _out(torch, torch.float64, n, 1))
+    _assert_equal("normal_f64 2^22 + 5", _host(out), orc.fill_normal_f64(7, first, n))
+
+
 def test_normal_f64_streams_share_the_miss_list(rng, torch, orc):
     """Fills on two streams use the same per-device miss list in turn."""
     n = 1 << 20
