@@ -92,13 +92,13 @@ def fill_specs():
           lambda r, o, f, s: r.rng_fill_normal_f32(W.NORMAL_SEED, f, o, s)),
         F("normal_f64", "float64", 8, 0, "zig_table_pass+zig_miss_pass", "normal_f64.cu",
           lambda r, o, f, s: r.rng_fill_normal_f64(W.NORMAL_SEED, f, o, s)),
-        F("dropout_fwd_p0.1", "x", 4, 4, "dropout_vec_kernel", "dropout.cu",
+        F("dropout_fwd_p0.1", "x", 4, 4, "dropout_v8_kernel", "dropout.cu",
           lambda r, o, f, s: r.rng_dropout_fwd(o[0], o[1], 0.1, W.DROPOUT_SEED, f, s)),
-        F("dropout_bwd_p0.1", "dy", 4, 4, "dropout_vec_kernel", "dropout.cu",
+        F("dropout_bwd_p0.1", "dy", 4, 4, "dropout_v8_kernel", "dropout.cu",
           lambda r, o, f, s: r.rng_dropout_bwd(o[0], o[1], 0.1, W.DROPOUT_SEED, f, s)),
-        F("dropout_fwd_p0.5", "x", 4, 4, "dropout_vec_kernel", "dropout.cu",
+        F("dropout_fwd_p0.5", "x", 4, 4, "dropout_v8_kernel", "dropout.cu",
           lambda r, o, f, s: r.rng_dropout_fwd(o[0], o[1], 0.5, W.DROPOUT_SEED, f, s)),
-        F("dropout_bwd_p0.5", "dy", 4, 4, "dropout_vec_kernel", "dropout.cu",
+        F("dropout_bwd_p0.5", "dy", 4, 4, "dropout_v8_kernel", "dropout.cu",
           lambda r, o, f, s: r.rng_dropout_bwd(o[0], o[1], 0.5, W.DROPOUT_SEED, f, s)),
     ]
 

@@ -65,15 +65,19 @@ def test_fill_writes_only_its_elements(rng, torch, orc, name):
 
 
 def test_dropout_writes_only_its_elements(rng, torch):
+    """y at every offset within 32 bytes, x aligned (the 32-byte kernel at
+    offset 0, the 16-byte one at offset 4, the scalar one otherwise) and x at
+    y's offset (the 32-byte kernel with a head of 0..7 elements)."""
     from dropout_lowbias32_hash32_gb300 import workloads
     for n in SIZES:
-        x = torch.from_numpy(workloads.dropout_x(max(n, 1))[:n]).cuda()
-        for offset in range(4):
-            buf = torch.full((GUARD + (offset + n) * 4 + GUARD,), CANARY, dtype=torch.uint8, device="cuda")
-            start = GUARD + offset * 4
-            y = buf[start:start + n * 4].view(torch.float32)
-            rng.rng_dropout_fwd(x, y, 0.3, 42, 0)  # x aligned, y at `offset` (the scalar kernel when they differ)
-            host = buf.cpu().numpy()
-            assert np.all(host[:start] == CANARY) and np.all(host[start + n * 4:] == CANARY), (n, offset)
-            if n >= 16:
-                assert not np.all(host[start:start + n * 4] == CANARY), (n, offset, "not written")
+        xh = torch.from_numpy(workloads.dropout_x(max(n, 1) + 8)).cuda()
+        for offset in range(8):
+            for x in (xh[:n], xh[offset:offset + n]):
+                buf = torch.full((GUARD + (offset + n) * 4 + GUARD,), CANARY, dtype=torch.uint8, device="cuda")
+                start = GUARD + offset * 4
+                y = buf[start:start + n * 4].view(torch.float32)
+                rng.rng_dropout_fwd(x, y, 0.3, 42, 0)
+                host = buf.cpu().numpy()
+                assert np.all(host[:start] == CANARY) and np.all(host[start + n * 4:] == CANARY), (n, offset)
+                if n >= 16:
+                    assert not np.all(host[start:start + n * 4] == CANARY), (n, offset, "not written")

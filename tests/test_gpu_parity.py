@@ -257,6 +257,25 @@ def test_dropout_mixed_alignment_takes_the_scalar_path(rng, torch, orc):
         _assert_equal(f"mixed offset {offset}", _host(y), orc.dropout(x, 0.5, 42, 5))
 
 
+def test_dropout_every_alignment(rng, torch, orc):
+    """Every offset of x within 32 bytes, with y at the same offset (32-byte
+    kernel), 16 bytes away (16-byte kernel) and 4 bytes away (scalar kernel),
+    and in place: every element equals the oracle's."""
+    n = 100003
+    x = workloads.dropout_x(n + 8)
+    for ox in range(8):
+        xs = x[ox:ox + n]
+        want = orc.dropout(xs, 0.3, 42, 7)
+        buf = torch.empty(n + 16, dtype=torch.float32, device="cuda")  # 256-byte aligned
+        buf[:n + 8].copy_(torch.from_numpy(x))
+        xg = buf[ox:ox + n]
+        for oy in (ox, (ox + 4) % 8, (ox + 1) % 8):
+            y = rng.rng_dropout_fwd(xg, _out(torch, torch.float32, n, oy), 0.3, 42, 7)
+            _assert_equal(f"x offset {ox}, y offset {oy}", _host(y), want)
+        rng.rng_dropout_fwd(xg, xg, 0.3, 42, 7)
+        _assert_equal(f"in place at offset {ox}", _host(xg), want)
+
+
 def test_slow_path_exp_log_bit_exact(rng, torch, orc):
     """The ziggurat slow path's own exp and log, layer by layer."""
     g = np.random.default_rng(4)
