@@ -551,7 +551,8 @@ def test_write_ceiling_hook_writes_what_it_states(rng, torch):
 
 
 def test_fill_longer_than_one_piece(rng, torch, orc):
-    """n > 2^31 is split into pieces of 2^31 elements; the seam is invisible."""
+    """n > 2^31 is split into pieces of 2^31 elements; the seam is invisible
+    (a fill, the ziggurat with its miss lists, and dropout with its input)."""
     n = (1 << 31) + 1000
     out = rng.rng_fill_u32(5, U32 - 7, torch.empty(n, dtype=torch.int32, device="cuda"))
     idx = np.concatenate([np.arange(0, 64), np.arange((1 << 31) - 64, (1 << 31) + 64), np.arange(n - 64, n),
@@ -563,6 +564,14 @@ def test_fill_longer_than_one_piece(rng, torch, orc):
     got = _host(out[torch.from_numpy(idx).cuda()])
     _assert_equal("normal_f64 > 2^31", got, orc.fill_normal_f64(7, 1, idx=idx))
     del out
+    torch.cuda.empty_cache()
+    # dropout reads its input piece by piece: x[i] = (i mod 1001) - 500, counters from first = 11
+    x = (torch.arange(n, device="cuda", dtype=torch.int64) % 1001 - 500).to(torch.float32)
+    y = rng.rng_dropout_fwd(x, torch.empty_like(x), 0.3, 42, 11)
+    got = _host(y[torch.from_numpy(idx).cuda()])
+    xs = ((idx % 1001) - 500).astype(np.float32)
+    _assert_equal("dropout > 2^31", got, orc.dropout(xs, 0.3, 42, 11, idx=idx))
+    del x, y
     torch.cuda.empty_cache()
 
 
