@@ -460,13 +460,14 @@ def run_ours(args):
     slow = {"fill": slowest.name, "kernel": slowest.kernel, "ms": fills[slowest.name]["ms"],
             "frac_of_hbm": fills[slowest.name]["frac_of_hbm"]}
     if slowest.name == "normal_f64":
-        # the fast path spends one DFMA per element; GB300 retires 2 DFMA per SM and cycle
+        # the fast path spends one DFMA on seven elements in eight (the eighth takes the exact
+        # integer product); GB300 retires 2 DFMA per SM and cycle
         props = torch.cuda.get_device_properties(dev)
         mhz = clocks.summary().get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
         fp64_peak = 2.0 * props.multi_processor_count * mhz * 1e6
-        dfma = n / (fill_ms["normal_f64"] / 1e3)
+        dfma = 7 / 8 * n / (fill_ms["normal_f64"] / 1e3)
         slow.update({"bound": "fp64", "achieved": round(dfma / 1e9, 1), "peak": round(fp64_peak / 1e9, 1),
-                     "unit": "G DFMA/s (one per element on the fast path)", "frac": round(dfma / fp64_peak, 3)})
+                     "unit": "G DFMA/s (7 per 8 elements on the fast path)", "frac": round(dfma / fp64_peak, 3)})
 
     next_rows = None
     if not args.no_next and not args.only:
