@@ -6,7 +6,8 @@
 // of draws miss the fast path and continue on a substream keyed by the
 // draw's global index, so a fill cut at any element equals the whole fill;
 // misses are queued locally and appended to a device list with one atomic
-// add (here: per-warp queues in shared memory, flushed 32 entries at a time);
+// add (here: per-warp queues in shared memory, flushed 32 entries at a time;
+// the few fast draws the integer product cannot round join them);
 // the second kernel takes one miss per thread and, if the list overflowed,
 // walks the whole fill again; the layer table is not in constant memory,
 // which serialises lanes that read different layers (here: the table pass
@@ -20,11 +21,13 @@
 //
 // Draw w = D64(seed, c): layer j = w & 1023, sign = bit 10, m = w >> 11 (53
 // bits); x = RNE((m 2^-53) X[j]); fast iff x < X[j+1].  GB300's FP64 pipe
-// retires 2 fma per SM and cycle (1/64 of FP32), so the fast path spends
-// exactly one FP64 instruction per element: t = 1 + (m mod 2^52) 2^-52 is
+// retires 2 fma per SM and cycle (1/64 of FP32), so the fast path spends at
+// most one FP64 instruction per element: t = 1 + (m mod 2^52) 2^-52 is
 // assembled from the draw's bits, and fma(t, X[j]/2, b ? 0 : -X[j]/2) with
 // b = bit 52 of m equals (m 2^-53) X[j] before its single rounding, so it
-// returns the IEEE product bit for bit.
+// returns the IEEE product bit for bit.  One element in eight takes the same
+// product in exact integer arithmetic instead (scaled_by_u53_int), which
+// moves work from the FP64 pipe to the ALU and FMA pipes.
 //
 // Miss of layer 0: the tail beyond r = X[1] (Marsaglia 1964: a = -log(U1)/r,
 // b = -log(U2), accept when 2b >= a^2, value r + a, U in (0, 1]).  Miss of
