@@ -217,7 +217,8 @@ def _counters_with_low23(orc, seed: int, word: int, targets, first_n: int = 1 <<
     """Counters c (< first_n / 2) whose uniform at 2c + word has the given 23-bit grid index."""
     key = (orc.path, seed, word, first_n)
     if key not in _LOW23_CACHE:
-        _LOW23_CACHE.clear()
+        if len(_LOW23_CACHE) >= 4:  # the pins use four (seed, word) pairs; 128 MiB each
+            _LOW23_CACHE.clear()
         _LOW23_CACHE[key] = orc.fill_u32(seed, word, first_n)[::2] & 0x7FFFFF
     d = _LOW23_CACHE[key]
     return {t: np.nonzero(d == t)[0] for t in targets}
