@@ -136,10 +136,12 @@ rng_status rng_fill_i64_range(uint32_t seed, uint32_t first_counter, size_t n, i
 /* out[i] = randn(seed, c_i) = sqrt(-2 ln(1 - u0)) cos(2 pi u1) with u0 =
  * uniform(seed, 2c_i), u1 = uniform(seed, 2c_i + 1) (Phobos "Random
  * numbers", section randn): one value per counter, the cosine branch of
- * Box-Muller, |out| <= sqrt(46 ln 2) ~ 5.648.  Computed in f32 with a
- * relative-accurate logarithm and the fast cosine on the angle shifted by
- * half a turn into [-pi, pi) (tandem-sycl "Design", section Normals); each
- * value is within 4e-6 (1 + |z|) of the exact z. */
+ * Box-Muller, |out| <= sqrt(46 ln 2) ~ 5.648.  Computed in f32: below u0 =
+ * 2^-7 the series (1 + u0)^2 - 1 of -2 ln(1 - u0), above it the hardware
+ * log2; the hardware square root; the hardware cosine on the angle 2 pi u1
+ * in [0, 2 pi) (no half-turn shift as in tandem-sycl "Design", section
+ * Normals: GB300's cosine is as accurate over the whole turn).  Each value is
+ * within 4e-6 (1 + |z|) of the exact z. */
 rng_status rng_fill_normal_f32(uint32_t seed, uint32_t first_counter, size_t n, float *out,
                                void *stream);
 
