@@ -18,10 +18,11 @@ U32 = 1 << 32
 FIRSTS = (0, 1, 3, U32 - 5)
 # 3 waves of the u32 fill (152 SMs x 8 blocks x 256 threads x 4 elements) + a ragged tail
 BIG = 3 * 152 * 8 * 256 * 4 + 13
-# around the vector width and around one block's run of every generator
-# (256 threads x 4 or 8 vectors x 16/sizeof(T) elements: 2048 .. 16384)
+# around the vector width, around one block's run of every generator (256
+# threads x 4, 8 or 16 vectors x 16/sizeof(T) elements: 2048 .. 32768) and
+# around 2^16 (the pages' small-fill cutoff; this library has none)
 SMALL = (1, 2, 3, 5, 15, 16, 17, 31, 33, 1000, 2047, 2048, 2049, 4095, 4096, 4097, 8191, 8192, 8193,
-         16383, 16384, 16385, 65537)
+         16383, 16384, 16385, 32767, 32768, 32769, 65535, 65536, 65537)
 
 
 @pytest.fixture(scope="module")
