@@ -4,7 +4,8 @@ The output slice sits inside a larger buffer pre-filled with a canary byte
 pattern; after the fill, every byte before and after the slice must still
 hold the canary (a stand-in for a bounds-checking sanitizer, which is not
 available here).  Sizes bracket the vector width and one block's run of each
-generator; offsets cover every start within a 16-byte vector."""
+generator (up to 32768 elements); offsets cover every start within a 16-byte
+vector (within 32 bytes for dropout)."""
 import numpy as np
 import pytest
 
@@ -14,7 +15,7 @@ pytestmark = pytest.mark.gpu
 U32 = 1 << 32
 CANARY = 0xA5
 GUARD = 4096  # bytes on each side
-SIZES = (0, 1, 3, 17, 2047, 2049, 4095, 4097, 8191, 8193, 16385, 3 * 152 * 8 * 256 * 4 + 13)
+SIZES = (0, 1, 3, 17, 2047, 2049, 4095, 4097, 8191, 8193, 16383, 16385, 32767, 32769, 3 * 152 * 8 * 256 * 4 + 13)
 NAMES = ["u32", "u64", "f32", "f64", "u32_below_1000", "u64_below_1000", "i32_range", "i64_range32", "i64_range",
          "normal_f64", "u8", "u16", "f16", "bool", "exponential_f32", "exponential_f64", "normal_f32_precise",
          "normal_f32", "normal_f32_pairs"]
