@@ -210,18 +210,35 @@ def pin_ranges_wrap(orc):
 
 
 # ------------------------------------------------------------------ randn --
-_LOW23_CACHE = {}
+_HASH_INV = (pow(2146121005, -1, U32), pow((-2073254261) % U32, -1, U32))
 
 
-def _counters_with_low23(orc, seed: int, word: int, targets, first_n: int = 1 << 26):
-    """Counters c (< first_n / 2) whose uniform at 2c + word has the given 23-bit grid index."""
-    key = (orc.path, seed, word, first_n)
-    if key not in _LOW23_CACHE:
-        if len(_LOW23_CACHE) >= 4:  # the pins use four (seed, word) pairs; 128 MiB each
-            _LOW23_CACHE.clear()
-        _LOW23_CACHE[key] = orc.fill_u32(seed, word, first_n)[::2] & 0x7FFFFF
-    d = _LOW23_CACHE[key]
-    return {t: np.nonzero(d == t)[0] for t in targets}
+def _unhash32(y: np.ndarray) -> np.ndarray:
+    """hash32^-1 of 32-bit words (uint64 array): the xorshifts and the odd
+    multipliers undone in reverse order (see pin_hash_bijective)."""
+    inv1, inv2 = (np.uint64(v) for v in _HASH_INV)
+    x = y ^ (y >> np.uint64(16))
+    x = (x * inv2) & np.uint64(0xFFFFFFFF)
+    x = x ^ (x >> np.uint64(15)) ^ (x >> np.uint64(30))
+    x = (x * inv1) & np.uint64(0xFFFFFFFF)
+    return x ^ (x >> np.uint64(16))
+
+
+def _counters_with_low23(orc, seed: int, word: int, targets):
+    """Counters c whose uniform at 2c + word has the given 23-bit grid index.
+    hash32 is a bijection, so they are constructed: for the 512 draws D = h
+    2^23 + t, the counter k = hash32^-1(D) ^ hash32(seed), and those of k's
+    parity are 2c + word (about 256 per target).  The oracle's draws at them
+    are checked to carry the target."""
+    key = np.uint64(orc.hash32(seed))
+    out = {}
+    for t in targets:
+        d = (np.arange(512, dtype=np.uint64) << np.uint64(23)) | np.uint64(t)
+        ks = _unhash32(d) ^ key
+        ks = ks[(ks & np.uint64(1)) == np.uint64(word)]
+        assert np.all((orc.fill_u32(seed, 0, idx=ks) & 0x7FFFFF) == t), (seed, word, t)
+        out[t] = np.sort(ks >> np.uint64(1)).astype(np.int64)
+    return out
 
 
 def pin_randn_special_angles(orc):
