@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -49,6 +50,8 @@ rng_status check_out(const T *p, size_t n, const char *name)
     if (p == nullptr) return fail(RNG_EINVAL, "%s is NULL with n = %zu", name, n);
     if (reinterpret_cast<uintptr_t>(p) % sizeof(T) != 0)
         return fail(RNG_EINVAL, "%s is not aligned to its %zu-byte element", name, sizeof(T));
+    if (n > (UINTPTR_MAX - reinterpret_cast<uintptr_t>(p)) / sizeof(T))
+        return fail(RNG_EINVAL, "%s + %zu elements runs past the end of the address space", name, n);
     return RNG_OK;
 }
 
@@ -367,6 +370,9 @@ rng_status rng_debug_write_ceiling(int which, void *buf, size_t bytes, void *str
     if (which != 0 && which != 1) return fail(RNG_EINVAL, "rng_debug_write_ceiling: which must be 0 or 1");
     if (bytes == 0) return RNG_OK;
     if (buf == nullptr) return fail(RNG_EINVAL, "rng_debug_write_ceiling: buf is NULL with bytes = %zu", bytes);
+    if (bytes > UINTPTR_MAX - reinterpret_cast<uintptr_t>(buf))
+        return fail(RNG_EINVAL, "rng_debug_write_ceiling: buf + %zu bytes runs past the end of the address space",
+                    bytes);
     t_error[0] = '\0';
     if (which == 0) {
         const cudaError_t e = cudaMemsetAsync(buf, 0x5A, bytes, RNG_STREAM(stream));

@@ -25,8 +25,9 @@
  *     2^32 (2^31 for the 64-bit and normal draws, which consume counters 2c
  *     and 2c + 1).
  *   - Errors.  RNG_EINVAL is returned before anything is enqueued: a NULL or
- *     misaligned pointer with n > 0, a bound of 0, p outside [0, 1) or NaN,
- *     partially overlapping input and output.  RNG_ECUDA reports an error
+ *     misaligned pointer with n > 0, a pointer whose n elements would run
+ *     past the end of the address space, a bound of 0, p outside [0, 1) or
+ *     NaN, partially overlapping input and output.  RNG_ECUDA reports an error
  *     returned by the CUDA runtime while enqueuing (launch failure, invalid
  *     stream); faults of the device work itself surface at the caller's next
  *     synchronisation, as for any CUDA kernel.  RNG_ENOMEM reports a failed
@@ -281,7 +282,8 @@ rng_status rng_debug_eval_f64(int which, const double *in, double *out, size_t n
  * the launch shape of the fills (buf 16-byte aligned, bytes a multiple of
  * 16).  buf is a caller-owned device buffer whose contents are overwritten;
  * stream-ordered on stream.  RNG_EINVAL for another which, buf == NULL with
- * bytes > 0, or (which = 1) a misaligned buf or size; bytes == 0 is a no-op. */
+ * bytes > 0, buf + bytes past the end of the address space, or (which = 1) a
+ * misaligned buf or size; bytes == 0 is a no-op. */
 rng_status rng_debug_write_ceiling(int which, void *buf, size_t bytes, void *stream);
 
 #ifdef __cplusplus

@@ -69,6 +69,18 @@ def test_misaligned_output_rejected(rng):
     assert "aligned" in rng.rng_last_error()
 
 
+def test_length_past_the_address_space_rejected(rng):
+    # pointers never dereferenced: the range check runs before anything is enqueued
+    assert rng.raw("rng_fill_u32")(1, 0, 1 << 62, 0x1000, None) == rng.RNG_EINVAL
+    assert "address space" in rng.rng_last_error()
+    assert rng.raw("rng_fill_u64")(1, 0, 1 << 61, 0x1000, None) == rng.RNG_EINVAL
+    assert rng.raw("rng_fill_u8")(1, 0, (1 << 64) - 0x1000, 0x1000, None) == rng.RNG_EINVAL
+    assert rng.raw("rng_fill_normal_f64")(1, 0, 1 << 61, 0x1000, None) == rng.RNG_EINVAL
+    assert rng.raw("rng_dropout_fwd")(0x1000, 0x2000, 0.5, 1, 0, 1 << 62, None) == rng.RNG_EINVAL
+    assert rng.raw("rng_debug_write_ceiling")(1, 0x1000, (1 << 64) - 16, None) == rng.RNG_EINVAL
+    assert "address space" in rng.rng_last_error()
+
+
 def test_zero_bound_rejected(rng):
     assert rng.raw("rng_fill_u32_below")(1, 0, 4, 0, 0x1000, None) == rng.RNG_EINVAL
     assert rng.raw("rng_fill_u64_below")(1, 0, 4, 0, 0x1000, None) == rng.RNG_EINVAL
