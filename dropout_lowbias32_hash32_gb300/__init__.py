@@ -116,10 +116,18 @@ def _stream(stream, t) -> int | None:
     return int(getattr(stream, "cuda_stream", stream)) or None
 
 
+def _on_device(t):
+    """The library launches on the CUDA runtime's current device: make it the
+    tensor's for the duration of a call."""
+    import torch
+    return torch.cuda.device(t.device)
+
+
 def _fill(name, kind, seed, first_counter, out, stream, *extra):
     p, n = _ptr(out, kind)
-    _check(getattr(_lib, name)(seed & 0xFFFFFFFF, first_counter & 0xFFFFFFFF, n, *extra, p,
-                               _stream(stream, out)), name)
+    with _on_device(out):
+        _check(getattr(_lib, name)(seed & 0xFFFFFFFF, first_counter & 0xFFFFFFFF, n, *extra, p,
+                                   _stream(stream, out)), name)
     return out
 
 
@@ -209,8 +217,11 @@ def _dropout(name, x, y, p, seed, first_counter, stream):
     py, ny = _ptr(y, "f32", "y")
     if n != ny:
         raise ValueError(f"{name}: x has {n} elements, y has {ny}")
-    _check(getattr(_lib, name)(px, py, float(p), seed & 0xFFFFFFFF, first_counter & 0xFFFFFFFF, n,
-                               _stream(stream, y)), name)
+    if x.device != y.device:
+        raise ValueError(f"{name}: x is on {x.device}, y on {y.device}")
+    with _on_device(y):
+        _check(getattr(_lib, name)(px, py, float(p), seed & 0xFFFFFFFF, first_counter & 0xFFFFFFFF, n,
+                                   _stream(stream, y)), name)
     return y
 
 
@@ -250,8 +261,9 @@ def rng_debug_write_ceiling(which: int, buf, stream=None):
     if not buf.is_contiguous():
         raise ValueError("rng_debug_write_ceiling: buf must be contiguous")
     nbytes = buf.numel() * buf.element_size()
-    _check(_lib.rng_debug_write_ceiling(which, buf.data_ptr(), nbytes, _stream(stream, buf)),
-           "rng_debug_write_ceiling")
+    with _on_device(buf):
+        _check(_lib.rng_debug_write_ceiling(which, buf.data_ptr(), nbytes, _stream(stream, buf)),
+               "rng_debug_write_ceiling")
     return buf
 
 
@@ -260,5 +272,8 @@ def rng_debug_eval_f64(which: int, inp, out, stream=None):
     po, no = _ptr(out, "f64", "out")
     if n != no:
         raise ValueError("in and out differ in length")
-    _check(_lib.rng_debug_eval_f64(which, pi, po, n, _stream(stream, out)), "rng_debug_eval_f64")
+    if inp.device != out.device:
+        raise ValueError(f"rng_debug_eval_f64: in is on {inp.device}, out on {out.device}")
+    with _on_device(out):
+        _check(_lib.rng_debug_eval_f64(which, pi, po, n, _stream(stream, out)), "rng_debug_eval_f64")
     return out
