@@ -35,8 +35,8 @@ struct GenF32 {
 };
 
 // (w >> 11) * 2^-53 for the 64-bit draw w = hi:lo, exactly, from integer
-// operations only (GB300's FP64 pipe is far too narrow for an HBM-speed
-// fill).  Clear the 11 bits below m = w >> 11, normalise on the high word so
+// operations only (GB300's FP64 pipe is too narrow to convert every element
+// of an HBM-speed fill).  Clear the 11 bits below m = w >> 11, normalise on the high word so
 // m's leading one reaches bit 63, take the 53-bit significand (implicit bit
 // at bit 52) and add the biased exponent 1021 - z below it; the implicit bit
 // carries one into the exponent field, giving 2^(-1-z) (1.f).  The high word
@@ -61,6 +61,22 @@ __device__ __forceinline__ double scaled_u53_candidate(Words w, bool &small)
     return __hiloint2double(static_cast<int>(sig_hi + ((1021u - z) << 20)), static_cast<int>(sig_lo));
 }
 
+// The same value with one FP64 instruction: t = 1 + (m mod 2^52) 2^-52 is
+// assembled from the word's bits and, with b the top bit of m,
+// fma(t, 1/2, b ? 0 : -1/2) = (m mod 2^52) 2^-53 + b/2 = m 2^-53, exact for
+// every m (no small case).  The integer conversion keeps the ALU pipe busy
+// while the FP64 pipe idles; sending one element of each pair through the
+// fma balances them (2 DFMA per SM and cycle carry half the elements at the
+// fill's speed; all of them would make the FP64 pipe the bound).
+__device__ __forceinline__ double scaled_u53_fma(Words w)
+{
+    const uint32_t t_lo = __funnelshift_r(w.lo, w.hi, 11);
+    const uint32_t t_hi = ((w.hi >> 11) & 0xFFFFFu) | 0x3FF00000u;
+    const uint32_t c_hi = ~static_cast<uint32_t>(static_cast<int32_t>(w.hi) >> 31) & 0xBFE00000u;  // -1/2 or 0
+    return __fma_rn(__hiloint2double(static_cast<int>(t_hi), static_cast<int>(t_lo)), 0.5,
+                    __hiloint2double(static_cast<int>(c_hi), 0));
+}
+
 __device__ __forceinline__ double scaled_u53_to_double(Words w)
 {
     bool small = false;
@@ -73,18 +89,18 @@ struct GenF64 {
     static constexpr uint32_t kVectorsPerThread = 16;  // measured at 2^28: 1.1 % faster than 8, 2 % than 4
     uint32_t key;
     __device__ T operator()(uint32_t c) const { return scaled_u53_to_double(draw64_words(key, c)); }
-    // both elements of a 16-byte vector, one branch on a zero high word
+    // both elements of a 16-byte vector: the first by the fma, the second by
+    // the integer conversion with its branch on a zero high word.  At 2^28,
+    // 0.290 ms against 0.303 with both integer (1/4 of the elements by the
+    // fma: 0.295; 3/8: 0.289; 5/8: 0.336, FP64-bound).
     __device__ Vec16<T> vec(uint32_t c0) const
     {
         const Words w0 = draw64_words(key, c0), w1 = draw64_words(key, c0 + 1u);
         bool small = false;
         Vec16<T> x;
-        x.v[0] = scaled_u53_candidate(w0, small);
+        x.v[0] = scaled_u53_fma(w0);
         x.v[1] = scaled_u53_candidate(w1, small);
-        if (__builtin_expect(small, 0)) {
-            x.v[0] = scaled_u53_to_double(w0);
-            x.v[1] = scaled_u53_to_double(w1);
-        }
+        if (__builtin_expect(small, 0)) x.v[1] = scaled_u53_to_double(w1);
         return x;
     }
 };
