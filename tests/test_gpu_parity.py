@@ -521,13 +521,18 @@ def test_zero_high_word_of_the_64_bit_draw(rng, torch, orc):
     """hash32(0) = 0, so draw32(seed, c) = 0 exactly at c = hash32(seed): for a
     seed with even hash32(seed) the 64-bit draw at c = hash32(seed) / 2 (and
     c + 2^31) has a zero high word, the one case in 2^32 the f64 conversions
-    take out of line.  Checked inside a 16-byte vector and in the head."""
+    take out of line.  Checked at both elements of a 16-byte vector (the f64
+    fill converts the first by an fma, the second by integer operations with
+    a branch for this case), in the peeled head and in the tail."""
     seeds = [s for s in range(1, 64) if orc.hash32(s) % 2 == 0][:3]
     assert seeds
     for seed in seeds:
         for c in (orc.hash32(seed) >> 1, (orc.hash32(seed) >> 1) + (1 << 31)):
             assert orc.fill_u64(seed, c, 1)[0] >> 32 == 0
-            for first, offset in ((c - 6, 0), (c - 5, 1), (c - 1, 0)):
+            # (first, offset): c at index 6 (a vector's first element), 1 (its
+            # second), 0 behind an 8-byte offset (the head), 4 behind it (a
+            # second element) and 63 behind it (the tail)
+            for first, offset in ((c - 6, 0), (c - 1, 0), (c, 1), (c - 4, 1), (c - 63, 1)):
                 first &= U32 - 1
                 got = _host(rng.rng_fill_f64(seed, first, _out(torch, torch.float64, 64, offset)))
                 assert np.array_equal(got.view(np.uint64), orc.fill_f64(seed, first, 64).view(np.uint64))
