@@ -126,11 +126,14 @@ def test_full_size_normal_f64_every_miss(rng, torch, orc):
     torch.cuda.empty_cache()
 
 
-def test_full_size_normal_f32(rng, torch, orc, sample):
+@pytest.mark.parametrize("first", [0, 3])
+def test_full_size_normal_f32(rng, torch, orc, sample, first):
+    """First counter 0 (the benchmark's) takes the aligned generator, 3 the
+    general one."""
     out = torch.empty(N, dtype=torch.float32, device="cuda")
-    rng.rng_fill_normal_f32(W.NORMAL_SEED, 3, out)
+    rng.rng_fill_normal_f32(W.NORMAL_SEED, first, out)
     z = _gather(torch, out, sample).astype(np.float64)
-    ref = orc.fill_randn(W.NORMAL_SEED, 3, idx=sample)
+    ref = orc.fill_randn(W.NORMAL_SEED, first, idx=sample)
     assert np.max(np.abs(z - ref) / (1 + np.abs(ref))) <= 4e-6
     # moments of the whole fill (on the device)
     zt = out.double()
@@ -138,6 +141,30 @@ def test_full_size_normal_f32(rng, torch, orc, sample):
     assert abs(zt.var().item() - 1) < 5 * math.sqrt(2 / N)
     assert zt.abs().max().item() <= math.sqrt(-2 * math.log(2.0 ** -23)) * (1 + 1e-6)
     del out, zt
+    torch.cuda.empty_cache()
+
+
+def test_normal_f32_large_ragged_fill(rng, torch, orc):
+    """A fill of 2^26 + 4101 elements behind a 4-byte offset, first counter 1:
+    a 3-element head, then the aligned generator's body of 2^24 + 1024
+    vectors, which ends in a partial block (a block covers 4096 or 8192
+    vectors), and a 2-element tail.  The elements around these boundaries
+    match the oracle; the element in front of the output is untouched."""
+    n = (1 << 26) + 4101
+    base = torch.full((n + 1,), float("nan"), dtype=torch.float32, device="cuda")
+    out = base[1:]
+    rng.rng_fill_normal_f32(W.NORMAL_SEED, 1, out)
+    body_end = 3 + 4 * ((n - 3) // 4)
+    last_block = 3 + 4 * 8192 * ((n - 3) // 4 // 8192)
+    idx = np.unique(np.concatenate([np.arange(0, 64), np.arange(last_block - 4096, n),
+                                    np.arange(3 + 4 * 4096 - 64, 3 + 4 * 4096 + 64),
+                                    np.arange(3 + 4 * 8192 - 64, 3 + 4 * 8192 + 64)]))
+    assert body_end == n - 2 and idx.max() == n - 1
+    z = _gather(torch, out, idx).astype(np.float64)
+    ref = orc.fill_randn(W.NORMAL_SEED, 1, idx=idx)
+    assert np.max(np.abs(z - ref) / (1 + np.abs(ref))) <= 4e-6
+    assert math.isnan(base[0].item())
+    del base, out
     torch.cuda.empty_cache()
 
 
