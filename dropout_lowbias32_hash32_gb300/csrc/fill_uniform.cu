@@ -86,7 +86,10 @@ __device__ __forceinline__ double scaled_u53_to_double(Words w)
 
 struct GenF64 {
     using T = double;
-    static constexpr uint32_t kVectorsPerThread = 16;  // measured at 2^28: 1.1 % faster than 8, 2 % than 4
+    // measured at 2^28 with half the conversions on the FP64 pipe: 0.279 ms
+    // against 0.285 at 4 and 0.289 at 16 (73 registers: the DFMA's latency
+    // wants the warps that 40 registers leave room for)
+    static constexpr uint32_t kVectorsPerThread = 8;
     uint32_t key;
     __device__ T operator()(uint32_t c) const { return scaled_u53_to_double(draw64_words(key, c)); }
     // both elements of a 16-byte vector: the first by the fma, the second by
