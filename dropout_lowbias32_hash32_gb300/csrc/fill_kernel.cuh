@@ -89,8 +89,19 @@ __device__ __forceinline__ Vec16<typename Gen::T> gen_vec(const Gen &gen, uint32
     }
 }
 
+// Blocks per SM a generator asks the compiler to fit, which sets its register
+// budget (`static constexpr int kMinBlocksPerSm`; default 0, no hint).
+template <class Gen, class = void>
+struct MinBlocksPerSm {
+    static constexpr int value = 0;
+};
 template <class Gen>
-__global__ void __launch_bounds__(kFillThreads)
+struct MinBlocksPerSm<Gen, decltype(void(Gen::kMinBlocksPerSm))> {
+    static constexpr int value = Gen::kMinBlocksPerSm;
+};
+
+template <class Gen>
+__global__ void __launch_bounds__(kFillThreads, MinBlocksPerSm<Gen>::value)
 fill_kernel(Gen gen, typename Gen::T *__restrict__ out, uint32_t first, uint32_t head, uint32_t n_vec,
             uint32_t n)
 {
