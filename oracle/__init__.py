@@ -61,6 +61,9 @@ _SIGS = {
     "orc_zig_table": (C.c_int, [C.c_uint, _p, _p, C.POINTER(_f64), C.POINTER(_f64)]),
     "orc_zig1024": (None, [_p, _p]),
     "orc_zig_first_draw_fast": (C.c_int, [_u32, _u32]),
+    "orc_substream_keys": (None, [_u32, C.c_int, _p, _sz, _p]),
+    "orc_substream_words32": (None, [_u32, _u32, _sz, _p]),
+    "orc_substream_words64": (None, [_u32, _u32, _sz, _p]),
     "orc_zig_candidates": (None, [_p, _sz, _p]),
     "orc_normal_f64": (_f64, [_u32, _u32]),
     "orc_fill_u32": (None, [_u32, _u32, _sz, _p, _p]),
@@ -164,6 +167,26 @@ class Oracle:
 
     def below64(self, seed: int, c: int, b: int) -> int:
         return self.lib.orc_below64(seed & 0xFFFFFFFF, c & 0xFFFFFFFF, b)
+
+    # Substreams (bounded retries and ziggurat misses) -------------------------
+    PURPOSES = ("B32", "B64", "N64")
+
+    def substream_keys(self, seed: int, purpose: str, counters) -> np.ndarray:
+        """The element keys of `counters` for one purpose ("B32", "B64", "N64")."""
+        g = np.ascontiguousarray(counters, dtype=np.uint32)
+        out = np.empty(g.size, np.uint32)
+        self.lib.orc_substream_keys(seed & 0xFFFFFFFF, self.PURPOSES.index(purpose), _ptr(g), g.size, _ptr(out))
+        return out
+
+    def substream_words32(self, key: int, n: int, k0: int = 0) -> np.ndarray:
+        out = np.empty(n, np.uint32)
+        self.lib.orc_substream_words32(key & 0xFFFFFFFF, k0 & 0xFFFFFFFF, n, _ptr(out))
+        return out
+
+    def substream_words64(self, key: int, n: int, k0: int = 0) -> np.ndarray:
+        out = np.empty(n, np.uint64)
+        self.lib.orc_substream_words64(key & 0xFFFFFFFF, k0 & 0xFFFFFFFF, n, _ptr(out))
+        return out
 
     def randn(self, seed: int, c: int) -> float:
         return self.lib.orc_randn(seed & 0xFFFFFFFF, c & 0xFFFFFFFF)

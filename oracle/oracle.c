@@ -159,6 +159,24 @@ static uint64_t substream64(uint32_t key, uint32_t k)
     return ((uint64_t)substream32(key, 2u * k) << 32) | (uint64_t)substream32(key, 2u * k + 1u);
 }
 
+/* For the pins: the element keys of counters g[0..n) for one purpose (which
+ * = 0 B32, 1 B64, 2 N64), and words k0 .. k0 + n - 1 of one element key. */
+void orc_substream_keys(uint32_t seed, int which, const uint32_t *g, size_t n, uint32_t *out)
+{
+    const uint32_t purpose = which == 0 ? PURPOSE_BELOW32 : which == 1 ? PURPOSE_BELOW64 : PURPOSE_NORMAL64;
+    for (size_t i = 0; i < n; ++i) out[i] = substream_key(seed, purpose, g[i]);
+}
+
+void orc_substream_words32(uint32_t key, uint32_t k0, size_t n, uint32_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = substream32(key, k0 + (uint32_t)i);
+}
+
+void orc_substream_words64(uint32_t key, uint32_t k0, size_t n, uint64_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = substream64(key, k0 + (uint32_t)i);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Bounded integers: Lemire's multiply-shift with rejection [PK; Tandem-P].  */
 /* ------------------------------------------------------------------------ */

@@ -765,6 +765,112 @@ def pin_zig_wedge_acceptance(orc):
     assert abs(accepted.mean() - expected) < 5 * sigma, (accepted.mean(), expected)
 
 
+# ------------------------------------------------------------ substreams --
+def _first_words32(orc, keys) -> np.ndarray:
+    return np.array([orc.substream_words32(int(k), 1)[0] for k in keys], dtype=np.uint32)
+
+
+def _corr(a: np.ndarray, b: np.ndarray) -> float:
+    return float(np.corrcoef(a.astype(np.float64), b.astype(np.float64))[0, 1])
+
+
+def pin_substream_purposes(orc):
+    """A draw that is rejected or misses continues on a substream of its own
+    purpose and its own counter (tandem-sycl "Design", Normals: split(g) of
+    sub(PURPOSE) of the key, g the draw's global index).  For one seed the
+    bounded-32, bounded-64 and normal-64 purposes give different element keys
+    at the same counter, different counters give different keys, and the
+    substreams' first words are uncorrelated with one another and with the
+    main stream's draws at and next to the element's own counter (equal only
+    at the 2^-32 chance rate)."""
+    n = 1 << 13
+    c0 = 12345
+    counters = np.arange(c0, c0 + n, dtype=np.uint32)
+    bound = 5 / math.sqrt(n)
+    for seed in (1, 7, 0x9E3779B9):
+        keys = {p: orc.substream_keys(seed, p, counters) for p in orc.PURPOSES}
+        for p in orc.PURPOSES:
+            assert np.unique(keys[p]).size == n, (seed, p)  # one key per counter
+        words = {p: _first_words32(orc, keys[p]) for p in orc.PURPOSES}
+        main = orc.fill_u32(seed, c0 - 2, n + 4)
+        for i, p in enumerate(orc.PURPOSES):
+            for q in orc.PURPOSES[i + 1:]:
+                assert np.count_nonzero(keys[p] == keys[q]) <= 1, (seed, p, q)
+                assert np.count_nonzero(words[p] == words[q]) <= 1, (seed, p, q)
+                assert abs(_corr(words[p], words[q])) < bound, (seed, p, q)
+            for shift in range(5):  # main-stream draws at c - 2 .. c + 2
+                near = main[shift:shift + n]
+                assert np.count_nonzero(words[p] == near) <= 1, (seed, p, shift)
+                assert abs(_corr(words[p], near)) < bound, (seed, p, shift)
+
+
+def pin_substream_is_the_generator(orc):
+    """A substream is the generator itself keyed by the element key K: its
+    32-bit word k is the draw at counter k of the seed s with hash32(s) = K,
+    and its 64-bit word k the 64-bit draw at counter k, whose high word is the
+    draw at 2k (the main stream's pinned word order), with the same counter
+    wrap."""
+    keys = [0, 1, 0xFFFFFFFF]
+    for p in orc.PURPOSES:
+        keys += [int(k) for k in orc.substream_keys(3, p, np.array([0, 77, U32 - 1], np.uint32))]
+    seeds = _unhash32(np.array(keys, dtype=np.uint64))
+    for key, s in zip(keys, (int(v) for v in seeds)):
+        assert orc.hash32(s) == key
+        assert np.array_equal(orc.substream_words32(key, 300), orc.fill_u32(s, 0, 300)), key
+        assert np.array_equal(orc.substream_words64(key, 300), orc.fill_u64(s, 0, 300)), key
+        assert np.array_equal(orc.substream_words32(key, 8, U32 - 4), orc.fill_u32(s, U32 - 4, 8)), key
+        k0 = (1 << 31) - 4  # the 64-bit words' counters 2k wrap here
+        assert np.array_equal(orc.substream_words64(key, 8, k0), orc.fill_u64(s, k0, 8)), key
+
+
+def _lemire_first(words, b: int, w: int):
+    """The first word of `words` that the exact-threshold Lemire step accepts,
+    and its value (brute-force integer arithmetic)."""
+    t = (1 << w) % b
+    for x in words:
+        prod = int(x) * b
+        if prod % (1 << w) >= t:
+            return prod >> w
+    return None
+
+
+def pin_retries_take_substream_words_in_order(orc):
+    """An element whose own draw the Lemire step rejects returns the first
+    accepted value among its substream's words 0, 1, 2, ... (bounds 2^31 + 1
+    and 2^63 + 1, where about half of all draws are rejected), and the retried
+    values are independent of the rejected first draw (8 x 8 contingency
+    table, chi-square)."""
+    for w, b, purpose, draws, fill, words in (
+            (32, (1 << 31) + 1, "B32", orc.fill_u32, orc.fill_u32_below, orc.substream_words32),
+            (64, (1 << 63) + 1, "B64", orc.fill_u64, orc.fill_u64_below, orc.substream_words64)):
+        seed, c0, n = 5, 100, 2048
+        d = draws(seed, c0, n)
+        v = fill(seed, c0, b, n)
+        keys = orc.substream_keys(seed, purpose, np.arange(c0, c0 + n, dtype=np.uint32))
+        rejected = 0
+        for i in range(n):
+            first = _lemire_first([d[i]], b, w)
+            if first is not None:
+                assert int(v[i]) == first, (w, i)
+                continue
+            rejected += 1
+            assert int(v[i]) == _lemire_first(words(int(keys[i]), 64), b, w), (w, i)
+        assert rejected > n // 3, (w, rejected)
+        # independence of the retried value from the rejected first draw
+        n = 1 << 16
+        d = draws(seed, 0, n)
+        v = fill(seed, 0, b, n)
+        top = w - 3
+        d_obj = d.astype(object)
+        rej = np.array([(int(x) * b) % (1 << w) < (1 << w) % b for x in d_obj])
+        first_bin = (d[rej] >> np.uint64(top) if w == 64 else d[rej] >> np.uint32(top)).astype(np.int64)
+        value_bin = (v[rej].astype(object) * 8 // b).astype(np.int64)
+        table = np.zeros((8, 8))
+        np.add.at(table, (first_bin, value_bin), 1)
+        table = table[table.sum(axis=1) > 0]
+        assert stats.chi2_contingency(table)[1] > 1e-4, w
+
+
 # ---------------------------------------------------------- slice invariant -
 def pin_slice_invariant(orc):
     """A fill cut at any element equals the whole fill (tandem-sycl 'Design',
@@ -815,5 +921,7 @@ ALL_PINS = [
     pin_neglog64_accuracy, pin_neglog64_table, pin_exponential_f64_fill,
     pin_dropout, pin_zexp_zlog,
     pin_zig_table_published, pin_zig_table_invariants, pin_zig_candidate_rounding, pin_zig_miss_rate,
-    pin_normal_f64_distribution, pin_zig_wedge_acceptance, pin_slice_invariant,
+    pin_normal_f64_distribution, pin_zig_wedge_acceptance,
+    pin_substream_purposes, pin_substream_is_the_generator, pin_retries_take_substream_words_in_order,
+    pin_slice_invariant,
 ]
