@@ -15,7 +15,8 @@ fill (CUDA events around each call on its stream); `roofline` relates the
 kernel with the largest share of the step to the measured HBM bandwidth and
 `slowest_fill` gives the slowest call with the pipe that bounds it;
 `next_rows` times the fills beyond the step (paired normals, narrow fills)
-one by one, outside `value`; `e2e`
+one by one, outside `value`; `configs` times the normals at 2^24 and 2^28
+from first counters 0, 1 and 3; `e2e`
 repeats the step through the same C ABI with pinned host buffers (inputs
 copied in, every output copied out, inside the timed region);
 `cpu_baseline` times the CPU oracle on a bounded sample.  Under torchrun
@@ -39,7 +40,20 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from dropout_lowbias32_hash32_gb300 import workloads as W  # noqa: E402
+
+
+def _load_workloads():
+    # by file path, so that the reference (oracle) arm does not run the
+    # package's __init__, which maps the CUDA library
+    import importlib.util
+    path = os.path.join(ROOT, "dropout_lowbias32_hash32_gb300", "workloads.py")
+    spec = importlib.util.spec_from_file_location("_lowbias32_workloads", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+W = _load_workloads()
 
 GIB = float(1 << 30)
 N = W.N_FULL
@@ -50,6 +64,8 @@ WORKLOAD = ("every fill at 2^28 elements per step: u32/u64/f32/f64 (seed 0x9E377
             "low+below32(1000) and i64 low+below64(1000) (low -500, seeds 1..4), normal_f32 and "
             "normal_f64 (seed 7), dropout fwd+bwd on X[2^20,256] at p=0.1 and 0.5 (seed 42)")
 CSRC = os.path.join(ROOT, "dropout_lowbias32_hash32_gb300", "csrc")
+# the arithmetic types the step's fills compute in and store
+DTYPE = "mixed: u32/u64/i32/i64 integer hashing, f32 and f64 arithmetic and outputs"
 
 
 # ---------------------------------------------------------------- the step --
@@ -492,6 +508,10 @@ def run_ours(args):
                                     "frac_of_hbm": round(gbs / peak, 3),
                                     "frac_of_write_ceiling": round(gbs / wpeak, 3), "kernel": spec.kernel}
 
+    configs = None
+    if not args.no_configs and not args.only:
+        configs = normals_configs(rng, torch, buf8, stream, dev, max(args.steps, 5), base)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(rng, torch, specs, outs, (host_x, host_dy), x, dy, n, stream, barrier, dist, dev,
@@ -502,14 +522,15 @@ def run_ours(args):
         result = {
             "metric": METRIC, "value": round(value, 1), "unit": "GiB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
             "data": "synthetic (counter-based fills need no input; dropout X ~ U(-1,1), dY ~ N(0,1) f32 "
                     "from numpy PCG64 seeds 11, 12)",
             "config": {"workload": WORKLOAD if not args.only else f"{args.only} at {n} elements",
                        "elements_per_fill": n, "fills_per_step": len(specs), "bytes_written_per_step": written,
                        "l2": "outputs of 1-2 GiB per fill exceed the 129 MB L2; no flush between steps",
                        "parallelism": f"counter-range shards x{world}"},
-            "fills": fills, "write_ceiling": ceiling, "roofline": roofline, "slowest_fill": slow, "next_rows": next_rows, "e2e": e2e,
+            "fills": fills, "write_ceiling": ceiling, "roofline": roofline, "slowest_fill": slow, "next_rows": next_rows,
+            "configs": configs, "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clocks.summary(),
             "cpu_baseline": None if args.no_cpu else cpu_baseline(specs),
@@ -518,6 +539,41 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return result
+
+
+def normals_configs(rng, torch, buf8, stream, dev, reps, base):
+    """The normals configuration rows: normal_f32 and normal_f64 (seed 7) at
+    2^24 and 2^28 elements from first counters 0, 1 and 3, each the median of
+    `reps` event-timed calls after 3 untimed ones.  Outputs of 2^24 elements
+    (64 and 128 MiB) fit in the 129 MB L2, so a 512 MiB buffer is written
+    between those timed calls (outside the events) to flush it; the 2^28
+    outputs are larger than L2."""
+    flush = torch.empty(1 << 29, dtype=torch.uint8, device=dev)
+    rows = []
+    for name, kind, written, fill in (
+            ("normal_f32", torch.float32, 4, rng.rng_fill_normal_f32),
+            ("normal_f64", torch.float64, 8, rng.rng_fill_normal_f64)):
+        for n in W.NORMAL_SIZES:
+            out = buf8.view(kind)[:n]
+            for first in (0, 1, 3):
+                c = (base + first) & 0xFFFFFFFF
+                for _ in range(3):
+                    fill(W.NORMAL_SEED, c, out, stream)
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(reps)]
+                for a, b in evs:
+                    if n * written <= (256 << 20):
+                        flush.zero_()
+                    a.record(stream)
+                    fill(W.NORMAL_SEED, c, out, stream)
+                    b.record(stream)
+                torch.cuda.synchronize()
+                ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+                rows.append({"fill": name, "elements": n, "first_counter": first, "ms": round(ms, 4),
+                             "gib_s_written": round(written * n / (ms / 1e3) / GIB, 1),
+                             "l2": "flushed between calls" if n * written <= (256 << 20) else "output > L2"})
+    del flush
+    return rows
 
 
 def write_ceiling(rng, torch, buf, stream, reps):
@@ -649,7 +705,7 @@ def run_reference(args):
     result = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GiB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 1),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic", "config": {"workload": WORKLOAD, "elements_per_fill": N,
                                         "reference_sample_per_fill": n_sample},
         "cpu_baseline": {"value": round(value, 4), "unit": "GiB/s", "cores": cores, "kind": "oracle",
@@ -673,6 +729,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the fills beyond the step")
+    ap.add_argument("--no-configs", action="store_true", help="skip the normals configuration rows")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("at least 3 warm-up steps")

@@ -616,7 +616,10 @@ static __device__ __align__(256) unsigned char
     g_noalloc_scratch[256 + (kNoAllocWedgeEntries + kNoAllocTailEntries) * sizeof(uint32_t)];
 
 // Device address of g_noalloc_scratch per device (host code cannot use the
-// symbol itself: on the host it names a stand-in, not device memory).
+// symbol itself: on the host it names a stand-in, not device memory).  Looked
+// up once per device and kept, like g_table_smem_set: both would be stale
+// after a cudaDeviceReset of the primary context, which the library does not
+// expect of its callers.
 std::atomic<unsigned char *> g_noalloc_addr[kNoAllocMaxDevices];
 std::atomic<unsigned> g_noalloc_sms[kNoAllocMaxDevices];
 

@@ -178,9 +178,10 @@ rng_status rng_fill_normal_f32_precise(uint32_t seed, uint32_t first_counter, si
  * X[1] (Marsaglia 1964), the others take the wedge test against exp(-x^2/2)
  * and otherwise start over with a fresh 64-bit word.  Both exp and log of
  * that path are fixed IEEE operation sequences, so the result is bit-exact
- * and reproducible.  The library keeps, per device, the layer table (in
- * global memory, 16 KiB) and the miss list (4 bytes per expected miss plus
- * slack), allocated on first use and held until the process exits; fills on
+ * and reproducible.  The layer tables are static device data of the library
+ * (no allocation).  The miss list (4 bytes per expected miss plus slack) is
+ * the one device allocation: made per device on first use, grown when a
+ * longer fill needs more, and held until the process exits; fills on
  * different streams that share it are ordered through its last event.  If
  * the list overflows, the second kernel walks the whole fill again. */
 rng_status rng_fill_normal_f64(uint32_t seed, uint32_t first_counter, size_t n, double *out,
@@ -199,6 +200,8 @@ rng_status rng_fill_normal_f64(uint32_t seed, uint32_t first_counter, size_t n, 
  *   - n must not exceed 2^28 elements; larger n returns RNG_EINVAL.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the rest of the process: it assumes that the
+ *     device's primary context is not reset (cudaDeviceReset) meanwhile.
  *   - Every call shares the array and clears its counter first: calls whose
  *     work overlaps on the GPU (other streams, other threads) race on it and
  *     give unspecified values.  Order them on one stream or with events.
@@ -208,16 +211,23 @@ rng_status rng_fill_normal_f64_noalloc(uint32_t seed, uint32_t first_counter, si
 
 /* ---- exponentials (tandem-sycl "Design", section Exponentials) ------------ */
 
-/* out[i] = -ln(1 - u), u = uniform(seed, c_i): 1 - u exact in (0, 1], within
- * 2 ulp of the exact value, in [0, 23 ln 2]. */
+/* out[i] = -ln(1 - u), u = uniform(seed, c_i): 1 - u = V 2^-23 exact in
+ * (0, 1], and the library's own table-driven binary32 logarithm of it
+ * (neg_log_grid in include/rng_device.cuh: exact reduction by 8-bit
+ * reciprocals, a TwoSum and a series to r^5, one final rounding), within
+ * 0.5035 ulp of the exact value on every input and reproducible bit for bit;
+ * in [0, 23 ln 2]. */
 rng_status rng_fill_exponential_f32(uint32_t seed, uint32_t first_counter, size_t n, float *out,
                                     void *stream);
 
-/* out[i] = 0 - zlog(1 - u), u = (D64(seed, c_i) >> 11) 2^-53: 1 - u exact, zlog
- * the library's own logarithm (x = 2^e m, m in (sqrt(1/2), sqrt 2], the atanh
- * series to s^23; the same fixed IEEE operations as the normal_f64 tail), so
- * the value is reproducible bit for bit and within 2 ulp of -ln(1 - u); in
- * [0, 53 ln 2].  FP64-bound on GB300 (about 26 FP64 operations per element). */
+/* out[i] = -ln(1 - u), u = (D64(seed, c_i) >> 11) 2^-53, by neglog64: a
+ * fixed-point logarithm in 32-, 64- and 128-bit integer arithmetic with no
+ * FP64 operation.  1 - u = V 2^-53 with the integer V = 2^53 - m is reduced
+ * exactly by 8-bit reciprocals, log1p of the reduced argument is a Horner
+ * series to r^7 in fixed point, the exponent and table terms are added at
+ * scale 2^96, and the sum is rounded once to binary64.  Within 0.5015 ulp of
+ * -ln(1 - u), reproducible bit for bit, in [0, 53 ln 2]; +0 at u = 0.  Bound
+ * by the integer pipes on GB300. */
 rng_status rng_fill_exponential_f64(uint32_t seed, uint32_t first_counter, size_t n, double *out,
                                     void *stream);
 
