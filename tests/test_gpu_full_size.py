@@ -104,6 +104,44 @@ def test_full_size_sampled(rng, torch, orc, sample, name, dtype, gpu, ref):
     torch.cuda.empty_cache()
 
 
+def test_full_size_exponential_f64_within_its_bound(rng, torch, orc, sample):
+    """The GPU's f64 exponential against a plain reference that shares nothing
+    with the own fixed-point logarithm: -log1p(-u) of u = (draw64 >> 11) 2^-53
+    in numpy's longdouble (x87 extended on x86-64, binary128 on aarch64),
+    within the stated 0.5025 ulp at every sampled element of the 2^28 fill."""
+    if np.finfo(np.longdouble).nmant < 63:
+        pytest.skip("needs a longdouble of at least 64 significand bits")
+    out = torch.empty(N, dtype=torch.float64, device="cuda")
+    rng.rng_fill_exponential_f64(W.NORMAL_SEED, 0, out)
+    y = _gather(torch, out, sample)
+    m = orc.fill_u64(W.NORMAL_SEED, 0, idx=sample) >> np.uint64(11)
+    ref = -np.log1p(-(m.astype(np.longdouble) / np.longdouble(2) ** 53))
+    zero = m == 0
+    assert np.all(y[zero] == 0) and not np.any(np.signbit(y[zero]))
+    err = np.abs(y[~zero].astype(np.longdouble) - ref[~zero]) / np.spacing(ref[~zero].astype(np.float64))
+    assert float(err.max()) <= 0.5025, float(err.max())
+    del out
+    torch.cuda.empty_cache()
+
+
+def test_full_size_normal_f32_precise_within_its_bound(rng, torch, orc, sample):
+    """The GPU's precise f32 normal against randn's plain binary64 value
+    (sqrt(-2 log(1 - u0)) cos(2 pi u1) in the C library's double functions),
+    independently of the own logarithm and cosine: within the stated 2.5 ulp
+    of binary32 at every sampled element, and 0 where u0 = 0."""
+    out = torch.empty(N, dtype=torch.float32, device="cuda")
+    rng.rng_fill_normal_f32_precise(W.NORMAL_SEED, 0, out)
+    z = _gather(torch, out, sample).astype(np.float64)
+    ref = orc.fill_randn(W.NORMAL_SEED, 0, idx=sample)
+    nz = ref != 0
+    ulp = np.spacing(np.abs(ref[nz]).astype(np.float32)).astype(np.float64)
+    worst = float(np.max(np.abs(z[nz] - ref[nz]) / ulp))
+    assert worst <= 2.5, worst
+    assert np.all(z[~nz] == 0)
+    del out
+    torch.cuda.empty_cache()
+
+
 def test_full_size_normal_f64_every_miss(rng, torch, orc):
     """Every element whose first draw misses (about 1.15 million at 2^28) is
     compared, and the list holds the oracle's misses and the few fast draws
