@@ -33,6 +33,18 @@ __device__ __forceinline__ Words draw64_words(uint32_t kf, uint32_t c)
 
 __device__ __forceinline__ uint64_t draw64(uint32_t kf, uint32_t c) { return lowbias32::draw64(lowbias32::Key{kf}, c); }
 
+// The 64-bit draws at an even counter c and at c + 1: the 32-bit draws at
+// 2c .. 2c + 3 differ only in their counter's low two bits, which never reach
+// the first xorshift's shifted term, so all four share it (the draw at 2c + k
+// starts from the one at 2c ^ k).
+__device__ __forceinline__ void draw64_pair_words(uint32_t kf, uint32_t c, Words &a, Words &b)
+{
+    const uint32_t x = c << 1;
+    const uint32_t f = x ^ (x >> 16) ^ kf;
+    a = Words{hash32_rounds(f), hash32_rounds(f ^ 1u)};
+    b = Words{hash32_rounds(f ^ 2u), hash32_rounds(f ^ 3u)};
+}
+
 // Substream of one element for retries and ziggurat misses: element key
 // hash32(c ^ purpose_key) with purpose_key = hash32(hash32(seed) ^ P) from
 // the host (passed folded); word k is hash32(k ^ element key).

@@ -319,12 +319,17 @@ def test_normal_f64_miss_list_overflow_walks_the_fill(rng, torch, orc):
     _assert_equal("default capacity", _host(out), want)
 
 
+# The share of the table pass's elements that take the exact integer product
+# instead of the fma (its kIntMask: this many of every eight).
+INT_PRODUCT_FRACTION = 2 / 8
+
+
 def deferred_bounds(n):
     """Bounds on the fast draws the table pass defers to the second kernel:
-    one element in eight takes the integer product, which defers a draw when
-    the 10 or 11 discarded bits it sees are exactly one half (probability
-    2^-10 or 2^-11), within 5 standard deviations."""
-    lo, hi = n / 8 * 2.0 ** -11, n / 8 * 2.0 ** -10
+    INT_PRODUCT_FRACTION of the elements take the integer product, which
+    defers a draw when the 10 or 11 discarded bits it sees are exactly one
+    half (probability 2^-10 or 2^-11), within 5 standard deviations."""
+    lo, hi = n * INT_PRODUCT_FRACTION * 2.0 ** -11, n * INT_PRODUCT_FRACTION * 2.0 ** -10
     return lo - 5 * math.sqrt(lo), hi + 5 * math.sqrt(hi) + 1e-5 * n
 
 
