@@ -74,31 +74,6 @@ __device__ __forceinline__ uint32_t below32_candidate(const Below32Args &a, uint
     return static_cast<uint32_t>(m >> 32);
 }
 
-// x b as (high, low) 64-bit words.  A bound below 2^32 (the same for every
-// thread of a launch, so the branch does not diverge) needs only the two
-// 32 x 32 -> 64 products of x's halves: x b = (x_hi b) 2^32 + x_lo b.
-__device__ __forceinline__ uint64_t mul_64(uint64_t x, uint64_t bound, uint64_t &low)
-{
-    if ((bound >> 32) == 0) {
-        const uint32_t b = static_cast<uint32_t>(bound);
-        const uint64_t p_lo = static_cast<uint64_t>(static_cast<uint32_t>(x)) * b;
-        const uint64_t p_hi = static_cast<uint64_t>(static_cast<uint32_t>(x >> 32)) * b;
-        const uint64_t mid = (p_lo >> 32) + static_cast<uint32_t>(p_hi);  // < 2^33
-        low = (mid << 32) | static_cast<uint32_t>(p_lo);
-        return (p_hi >> 32) + (mid >> 32);
-    }
-    low = x * bound;
-    return __umul64hi(x, bound);
-}
-
-__device__ __forceinline__ uint64_t below64_candidate(const Below64Args &a, uint32_t c, bool &reject)
-{
-    uint64_t low;
-    const uint64_t high = mul_64(draw64(a.key, c), a.bound, low);
-    reject |= low < a.threshold;
-    return high;
-}
-
 // A 16-byte vector of a bounded fill: every element's candidate and one
 // branch on the OR of their rejection tests (rare: about 4 (2^w mod b) / 2^w
 // per vector), whose slow path recomputes the vector element by element with
@@ -127,13 +102,76 @@ struct GenBelow32 {
     __device__ Vec16<T> vec(uint32_t c0) const { return bounded_vec(*this, c0); }
 };
 
+// The 64-bit generators' vector: both elements' draws at once (for an even
+// first counter the four 32-bit draws share one first xorshift) and the
+// candidates.  kMode 0: bound below 2^32, so x b = (x_hi b + (x_lo b >> 32))
+// 2^32 + lo(x_lo b) by two 32 x 32 -> 64 multiply-adds, and the value (< b)
+// is the high word of the second; kMode 1: a 64-bit bound whose threshold
+// 2^64 mod b is below 2^32; kMode 2: a threshold of 64 bits (the 64-bit
+// products by the compiler's 64 x 64 forms, which measured faster than an
+// explicit chain of 32-bit multiply-adds).  With a threshold below 2^32 a
+// rejection needs the product's low 64 bits to have a zero high word, so the
+// vector's test is that word against zero (2^-32 of elements, exactly
+// rechecked by the slow path) instead of a 64-bit compare.
+// kEven and kMode are the same for every vector of a launch (the host picks
+// the instantiation); every value equals below64's.
+template <uint32_t kMode>
+__device__ __forceinline__ uint64_t below64_candidate_words(Words x, uint64_t bound, uint64_t threshold, bool &reject)
+{
+    const uint32_t b_lo = static_cast<uint32_t>(bound), b_hi = static_cast<uint32_t>(bound >> 32);
+    const uint64_t p0 = static_cast<uint64_t>(x.lo) * b_lo;
+    if constexpr (kMode == 0) {
+        const uint64_t p1 = static_cast<uint64_t>(x.hi) * b_lo + (p0 >> 32);
+        reject |= static_cast<uint32_t>(p1) == 0u;
+        return p1 >> 32;
+    } else {
+        (void)p0;
+        const uint64_t xx = (static_cast<uint64_t>(x.hi) << 32) | x.lo;
+        const uint64_t low = xx * bound;
+        if constexpr (kMode == 1) {
+            reject |= static_cast<uint32_t>(low >> 32) == 0u;
+        } else {
+            reject |= low < threshold;
+        }
+        return __umul64hi(xx, bound);
+    }
+}
+
+// Mode of a 64-bit bound (see below64_candidate_words).
+inline uint32_t below64_mode(const Below64Args &a)
+{
+    return (a.bound >> 32) == 0 ? 0u : ((a.threshold >> 32) == 0 ? 1u : 2u);
+}
+
+template <class Gen, bool kEven, uint32_t kMode>
+__device__ __forceinline__ Vec16<typename Gen::T> bounded64_vec(const Gen &gen, uint32_t c0)
+{
+    Words w0, w1;
+    if constexpr (kEven) {
+        draw64_pair_words(gen.a.key, c0, w0, w1);
+    } else {
+        w0 = draw64_words(gen.a.key, c0);
+        w1 = draw64_words(gen.a.key, c0 + 1u);
+    }
+    bool reject = false;
+    Vec16<typename Gen::T> x;
+    x.v[0] = gen.finish(below64_candidate_words<kMode>(w0, gen.a.bound, gen.a.threshold, reject));
+    x.v[1] = gen.finish(below64_candidate_words<kMode>(w1, gen.a.bound, gen.a.threshold, reject));
+    if (__builtin_expect(reject, 0)) {
+        x.v[0] = gen(c0);
+        x.v[1] = gen(c0 + 1u);
+    }
+    return x;
+}
+
+template <bool kEven, uint32_t kMode>
 struct GenBelow64 {
     using T = uint64_t;
     static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
     Below64Args a;
     __device__ T operator()(uint32_t c) const { return below64(a, c); }
-    __device__ T candidate(uint32_t c, bool &reject) const { return below64_candidate(a, c, reject); }
-    __device__ Vec16<T> vec(uint32_t c0) const { return bounded_vec(*this, c0); }
+    __device__ T finish(uint64_t v) const { return v; }
+    __device__ Vec16<T> vec(uint32_t c0) const { return bounded64_vec<GenBelow64, kEven, kMode>(*this, c0); }
 };
 
 // low + below, wrapped in two's complement (unsigned addition, then the
@@ -169,6 +207,7 @@ struct GenI64Range32 {
     __device__ Vec16<T> vec(uint32_t c0) const { return bounded_vec(*this, c0); }
 };
 
+template <bool kEven, uint32_t kMode>
 struct GenI64Range {
     using T = int64_t;
     static constexpr uint32_t kVectorsPerThread = kHeavyVectorsPerThread;
@@ -178,12 +217,26 @@ struct GenI64Range {
     {
         return static_cast<int64_t>(static_cast<uint64_t>(low) + below64(a, c));
     }
-    __device__ T candidate(uint32_t c, bool &reject) const
-    {
-        return static_cast<int64_t>(static_cast<uint64_t>(low) + below64_candidate(a, c, reject));
-    }
-    __device__ Vec16<T> vec(uint32_t c0) const { return bounded_vec(*this, c0); }
+    __device__ T finish(uint64_t v) const { return static_cast<int64_t>(static_cast<uint64_t>(low) + v); }
+    __device__ Vec16<T> vec(uint32_t c0) const { return bounded64_vec<GenI64Range, kEven, kMode>(*this, c0); }
 };
+
+// Launch a 64-bit generator family G<kEven, kMode> for a's bound: the body's
+// vectors start at counters first + head + 2v, even for all or for none.
+template <template <bool, uint32_t> class G, class... Extra>
+cudaError_t launch_below64_family(const Below64Args &a, uint32_t first, uint32_t n, typename G<true, 0>::T *out,
+                                  cudaStream_t s, Extra... extra)
+{
+    const bool even = ((first + head_elems<typename G<true, 0>::T>(out, n)) & 1u) == 0u;
+    switch (below64_mode(a) + (even ? 0u : 3u)) {
+    case 0: return launch_fill(G<true, 0>{a, extra...}, out, first, n, s);
+    case 1: return launch_fill(G<true, 1>{a, extra...}, out, first, n, s);
+    case 2: return launch_fill(G<true, 2>{a, extra...}, out, first, n, s);
+    case 3: return launch_fill(G<false, 0>{a, extra...}, out, first, n, s);
+    case 4: return launch_fill(G<false, 1>{a, extra...}, out, first, n, s);
+    default: return launch_fill(G<false, 2>{a, extra...}, out, first, n, s);
+    }
+}
 
 }  // namespace
 
@@ -196,7 +249,7 @@ cudaError_t launch_fill_u32_below(const Below32Args &a, uint32_t first, uint32_t
 cudaError_t launch_fill_u64_below(const Below64Args &a, uint32_t first, uint32_t n, uint64_t *out,
                                   cudaStream_t s)
 {
-    return launch_fill(GenBelow64{a}, out, first, n, s);
+    return launch_below64_family<GenBelow64>(a, first, n, out, s);
 }
 
 cudaError_t launch_fill_i32_range(const Below32Args &a, int32_t low, uint32_t first, uint32_t n,
@@ -214,7 +267,7 @@ cudaError_t launch_fill_i64_range32(const Below32Args &a, int64_t low, uint32_t 
 cudaError_t launch_fill_i64_range(const Below64Args &a, int64_t low, uint32_t first, uint32_t n,
                                   int64_t *out, cudaStream_t s)
 {
-    return launch_fill(GenI64Range{a, low}, out, first, n, s);
+    return launch_below64_family<GenI64Range>(a, first, n, out, s, low);
 }
 
 }  // namespace rngk

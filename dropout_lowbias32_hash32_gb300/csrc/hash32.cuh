@@ -33,6 +33,23 @@ __device__ __forceinline__ Words draw64_words(uint32_t kf, uint32_t c)
 
 __device__ __forceinline__ uint64_t draw64(uint32_t kf, uint32_t c) { return lowbias32::draw64(lowbias32::Key{kf}, c); }
 
+// d = a b + c (low or high 32 bits of the product) as one multiply-add, on
+// the FMA pipe.  A multiplier that is a kernel argument keeps the compiler
+// from turning a product by a power of two back into a shift on the ALU pipe:
+// mad_hi(x, 2^(32 - s), c) is (x >> s) + c.
+__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // The 64-bit draws at an even counter c and at c + 1: the 32-bit draws at
 // 2c .. 2c + 3 differ only in their counter's low two bits, which never reach
 // the first xorshift's shifted term, so all four share it (the draw at 2c + k

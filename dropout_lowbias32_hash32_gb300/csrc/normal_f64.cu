@@ -161,22 +161,6 @@ __device__ __forceinline__ bool scaled_by_u53_int(Words w, double half_v, uint64
     return scaled_by_u53_int<false>(w, v_hi, v_lo, significand_hi(v_hi, v_lo), bits);
 }
 
-// d = a b + c (low or high 32 bits of the product) as one multiply-add, on
-// the FMA pipe.  A multiplier that is a kernel argument keeps the compiler
-// from turning a product by a power of two back into a shift on the ALU pipe.
-__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 // Powers of two for mad_lo / mad_hi, passed to the table pass as an argument.
 struct Pow2 {
     uint32_t p20, p21;
