@@ -94,19 +94,19 @@ def fill_specs():
           lambda r, o, f, s: r.rng_fill_u32_below(1, f, 1000, o, s)),
         F("u32_below_2^32-2", "int32", 4, 0, "fill_kernel<GenBelow32>", "fill_bounded.cu",
           lambda r, o, f, s: r.rng_fill_u32_below(2, f, b32, o, s)),
-        F("u64_below_1000", "int64", 8, 0, "fill_kernel<GenBelow64>", "fill_bounded.cu",
+        F("u64_below_1000", "int64", 8, 0, "fill_kernel<GenBelow64<1, 0>>", "fill_bounded.cu",
           lambda r, o, f, s: r.rng_fill_u64_below(3, f, 1000, o, s)),
-        F("u64_below_2^64-2", "int64", 8, 0, "fill_kernel<GenBelow64>", "fill_bounded.cu",
+        F("u64_below_2^64-2", "int64", 8, 0, "fill_kernel<GenBelow64<1, 1>>", "fill_bounded.cu",
           lambda r, o, f, s: r.rng_fill_u64_below(4, f, b64, o, s)),
         F("i32_range", "int32", 4, 0, "fill_kernel<GenI32Range>", "fill_bounded.cu",
           lambda r, o, f, s: r.rng_fill_i32_range(1, f, W.LOW, 1000, o, s)),
         F("i64_range32", "int64", 8, 0, "fill_kernel<GenI64Range32>", "fill_bounded.cu",
           lambda r, o, f, s: r.rng_fill_i64_range32(2, f, W.LOW, 1000, o, s)),
-        F("i64_range", "int64", 8, 0, "fill_kernel<GenI64Range>", "fill_bounded.cu",
+        F("i64_range", "int64", 8, 0, "fill_kernel<GenI64Range<1, 0>>", "fill_bounded.cu",
           lambda r, o, f, s: r.rng_fill_i64_range(3, f, W.LOW, 1000, o, s)),
-        F("normal_f32", "float32", 4, 0, "fill_kernel<GenNormalF32<true>>", "normal_f32.cu",
+        F("normal_f32", "float32", 4, 0, "fill_kernel<GenNormalF32<1>>", "normal_f32.cu",
           lambda r, o, f, s: r.rng_fill_normal_f32(W.NORMAL_SEED, f, o, s)),
-        F("normal_f64", "float64", 8, 0, "zig_table_pass+zig_miss_pass", "normal_f64.cu",
+        F("normal_f64", "float64", 8, 0, "zig_table_pass<1>+zig_miss_pass", "normal_f64.cu",
           lambda r, o, f, s: r.rng_fill_normal_f64(W.NORMAL_SEED, f, o, s)),
         F("dropout_fwd_p0.1", "x", 4, 4, "dropout_v8_kernel", "dropout.cu",
           lambda r, o, f, s: r.rng_dropout_fwd(o[0], o[1], 0.1, W.DROPOUT_SEED, f, s)),

@@ -202,6 +202,22 @@ __device__ __forceinline__ FastDraw zig_fast(Words w)
     return d;
 }
 
+// zig_fast with the product by the integer form where it decides (the fma
+// where it defers): the same values, with no FP64 instruction in the
+// common case.
+__device__ __forceinline__ double scaled_by_u53_any(Words w, double half_v);
+__device__ __forceinline__ FastDraw zig_fast_int(Words w)
+{
+    const uint32_t j = w.lo & (kLayers - 1u);
+    const double2 e = __ldg(&kZigHalfXNext[j]);
+    const uint64_t xb = static_cast<uint64_t>(__double_as_longlong(scaled_by_u53_any(w, e.x)));
+    FastDraw d;
+    d.fast = xb < static_cast<uint64_t>(__double_as_longlong(e.y));
+    d.bits = xb | (static_cast<uint64_t>(w.lo & 0x400u) << 53);
+    d.base = j == 0;
+    return d;
+}
+
 // ---- slow path --------------------------------------------------------------
 
 // ((w >> 11) + 1) 2^-53, in (0, 1]
@@ -309,8 +325,9 @@ __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint3
 // the rest of its 32-byte sector back from HBM (a read-modify-write at a
 // random address for every miss; that, not the slow path, set the miss
 // pass's time).  So the other three elements of e's sector are recomputed by
-// the fma fast path, whose values equal the table pass's, and the four are
-// stored as one 32-byte sector.  If a neighbour also missed (about 1.3 % of
+// the fast path (the integer product, which leaves the FP64 pipe to the slow
+// path; the fma where it defers), whose values equal the table pass's, and
+// the four are stored as one 32-byte sector.  If a neighbour also missed (about 1.3 % of
 // sectors) or the sector runs past either end of the fill, only e is stored:
 // the neighbour's own thread writes its value.
 __device__ __forceinline__ void store_resolved(double *__restrict__ out, uint32_t n, uint32_t key, uint32_t first,
@@ -326,7 +343,7 @@ __device__ __forceinline__ void store_resolved(double *__restrict__ out, uint32_
             if (k == pos) {
                 b[k] = static_cast<unsigned long long>(__double_as_longlong(v));
             } else {
-                const FastDraw d = zig_fast(draw64_words(key, first + s0 + k));
+                const FastDraw d = zig_fast_int(draw64_words(key, first + s0 + k));
                 b[k] = d.bits;
                 all = all && d.fast;
             }
