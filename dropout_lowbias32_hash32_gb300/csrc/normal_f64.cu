@@ -277,6 +277,13 @@ __device__ __forceinline__ double scaled_by_u53_any(Words w, double half_v)
     return scaled_by_u53(w, half_v);
 }
 
+// x with its sign bit set when neg, by an integer operation (a negation of a
+// double may otherwise take GB300's narrow FP64 pipe)
+__device__ __forceinline__ double with_sign(double x, bool neg)
+{
+    return __longlong_as_double(__double_as_longlong(x) | (static_cast<long long>(neg) << 63));
+}
+
 __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint32_t c)
 {
     Words w = draw64_words(key, c);
@@ -287,7 +294,7 @@ __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint3
         const bool neg = w.lo & 0x400u;
         const double2 e = __ldg(&kZigHalfXNext[j]);
         const double x = scaled_by_u53_any(w, e.x);
-        if (__double_as_longlong(x) < __double_as_longlong(e.y)) return neg ? -x : x;
+        if (__double_as_longlong(x) < __double_as_longlong(e.y)) return with_sign(x, neg);
         if (j == 0) {
             const double r = kZigX[1];
             for (uint32_t t = 0; t < kMaxRounds; ++t) {
@@ -298,7 +305,7 @@ __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint3
                 const double b = -zlog(u2);
                 if (__dadd_rn(b, b) >= __dmul_rn(a, a)) {
                     const double z = __dadd_rn(r, a);
-                    return neg ? -z : z;
+                    return with_sign(z, neg);
                 }
             }
             break;
@@ -307,10 +314,10 @@ __device__ __noinline__ double zig_slow(uint32_t key, uint32_t normal_key, uint3
         const Words u = draw64_words(skf, k);
         k += 1u;
         const int screen = wedge_screen(x, f, u);
-        if (screen > 0) return neg ? -x : x;
+        if (screen > 0) return with_sign(x, neg);
         if (screen == 0) {
             const double y = __dadd_rn(f.x, scaled_by_u53(u, f.y));
-            if (y < zexp(__dmul_rn(__dmul_rn(x, x), -0.5))) return neg ? -x : x;
+            if (y < zexp(__dmul_rn(__dmul_rn(x, x), -0.5))) return with_sign(x, neg);
         }
         w = draw64_words(skf, k);
         k += 1u;
