@@ -1,6 +1,8 @@
-// hash32.cuh -- the library kernels' view of the public device header
-// (include/rng_device.cuh): the same lowbias32 functions, taking the
-// seed's folded key as a plain 32-bit value.
+// hash32.cuh -- the library kernels' draw helpers beyond the public device
+// header (include/rng_device.cuh): adapters that take the seed's folded key
+// as a plain 32-bit kernel argument, the substreams of bounded retries and
+// ziggurat misses, the paired 64-bit draws of an even counter, and the
+// multiply-adds that keep shifts off the ALU pipe.
 #pragma once
 
 #include <cstdint>
@@ -10,17 +12,10 @@
 namespace rngk {
 
 using lowbias32::hash32;
-using lowbias32::hash32_rounds;
 using lowbias32::Words;
 
 // The key k folded into the first xorshift of hash32(c ^ k).
 __host__ __device__ __forceinline__ uint32_t fold_key(uint32_t k) { return lowbias32::key_of_hash(k).folded; }
-
-// hash32(c ^ k) from the folded key kf.
-__device__ __forceinline__ uint32_t hash32_keyed(uint32_t kf, uint32_t c)
-{
-    return lowbias32::draw32(lowbias32::Key{kf}, c);
-}
 
 // The 32-bit draw at counter c (kf: the folded hash of the seed).
 __device__ __forceinline__ uint32_t draw32(uint32_t kf, uint32_t c) { return lowbias32::draw32(lowbias32::Key{kf}, c); }
@@ -58,14 +53,14 @@ __device__ __forceinline__ void draw64_pair_words(uint32_t kf, uint32_t c, Words
 {
     const uint32_t x = c << 1;
     const uint32_t f = x ^ (x >> 16) ^ kf;
-    a = Words{hash32_rounds(f), hash32_rounds(f ^ 1u)};
-    b = Words{hash32_rounds(f ^ 2u), hash32_rounds(f ^ 3u)};
+    a = Words{lowbias32::hash32_rounds(f), lowbias32::hash32_rounds(f ^ 1u)};
+    b = Words{lowbias32::hash32_rounds(f ^ 2u), lowbias32::hash32_rounds(f ^ 3u)};
 }
 
 // Substream of one element for retries and ziggurat misses: element key
 // hash32(c ^ purpose_key) with purpose_key = hash32(hash32(seed) ^ P) from
 // the host (passed folded); word k is hash32(k ^ element key).
-__device__ __forceinline__ uint32_t substream_key(uint32_t purpose_kf, uint32_t c) { return hash32_keyed(purpose_kf, c); }
+__device__ __forceinline__ uint32_t substream_key(uint32_t purpose_kf, uint32_t c) { return draw32(purpose_kf, c); }
 
 __device__ __forceinline__ uint32_t substream32(uint32_t skey, uint32_t k) { return hash32(k ^ skey); }
 
