@@ -322,12 +322,16 @@ __device__ __forceinline__ float small_uint_to_float(uint32_t x)
 }
 }  // namespace detail
 
-__device__ __forceinline__ float neg_log_grid(uint32_t m)
+// neg_log_grid with the table row j = round((M - 1) 256) fetched by load(j)
+// (a copy of detail::kNegLogTable elsewhere, e.g. in shared memory): the same
+// operations, so the same bits.
+template <class Load>
+__device__ __forceinline__ float neg_log_grid_by(uint32_t m, Load load)
 {
     const uint32_t bits = __float_as_uint(detail::small_uint_to_float(0x800000u - m));  // V, exact
     const uint32_t mant = bits & 0x7FFFFFu;
     const float M = __uint_as_float(mant | 0x3F800000u);
-    const float4 t = __ldg(&detail::kNegLogTable[(mant + 16384u) >> 15]);  // {inv_j, hi_j, lo_j, 0}
+    const float4 t = load((mant + 16384u) >> 15);  // {inv_j, hi_j, lo_j, 0}
     const float E = detail::small_uint_to_float(150u - (bits >> 23));      // 23 - k
     const float r = __fmaf_rn(M, t.x, -1.0f);
     const float t_hi = __fmaf_rn(E, detail::kNegLogLn2Hi, t.y);
@@ -342,6 +346,11 @@ __device__ __forceinline__ float neg_log_grid(uint32_t m)
     return __fadd_rn(s, __fadd_rn(__fadd_rn(err, t_lo), tail));
 }
 
+__device__ __forceinline__ float neg_log_grid(uint32_t m)
+{
+    return neg_log_grid_by(m, [](uint32_t j) { return __ldg(&detail::kNegLogTable[j]); });
+}
+
 // -ln(1 - u) for u = uniform(k, c), by neg_log_grid; in [0, 23 ln 2].
 __device__ __forceinline__ float exponential(Key k, uint32_t c) { return neg_log_grid(draw32(k, c) & 0x7FFFFFu); }
 
@@ -350,7 +359,9 @@ namespace detail {
 // target has them (each lane rounded like the scalar step, so the values are
 // neg_log_grid's bit for bit).  -r - bb is formed as -(r + bb), the same
 // value with the same sign of zero, since RN is symmetric.
-__device__ __forceinline__ float2 neg_log_grid_x2(uint32_t ma, uint32_t mb)
+// neg_log_grid_x2 with the table rows fetched by load(j), as neg_log_grid_by.
+template <class Load>
+__device__ __forceinline__ float2 neg_log_grid_x2_by(uint32_t ma, uint32_t mb, Load load)
 {
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 1000
     const float2 V = f32x2_unpack(f32x2_sub(f32x2_pack(__uint_as_float(0x4B000000u | (0x800000u - ma)),
@@ -358,8 +369,8 @@ __device__ __forceinline__ float2 neg_log_grid_x2(uint32_t ma, uint32_t mb)
                                             f32x2_pack(8388608.0f, 8388608.0f)));
     const uint32_t bits_a = __float_as_uint(V.x), bits_b = __float_as_uint(V.y);
     const uint32_t mant_a = bits_a & 0x7FFFFFu, mant_b = bits_b & 0x7FFFFFu;
-    const float4 ta = __ldg(&kNegLogTable[(mant_a + 16384u) >> 15]);
-    const float4 tb = __ldg(&kNegLogTable[(mant_b + 16384u) >> 15]);
+    const float4 ta = load((mant_a + 16384u) >> 15);
+    const float4 tb = load((mant_b + 16384u) >> 15);
     const unsigned long long M = f32x2_pack(__uint_as_float(mant_a | 0x3F800000u), __uint_as_float(mant_b | 0x3F800000u));
     const unsigned long long E = f32x2_sub(f32x2_pack(__uint_as_float(0x4B000000u | (150u - (bits_a >> 23))),
                                                       __uint_as_float(0x4B000000u | (150u - (bits_b >> 23)))),
@@ -380,8 +391,13 @@ __device__ __forceinline__ float2 neg_log_grid_x2(uint32_t ma, uint32_t mb)
     const unsigned long long tail = f32x2_pack(__fmul_rn(rr.x, pf.x), __fmul_rn(rr.y, pf.y));
     return f32x2_unpack(f32x2_add(s, f32x2_add(f32x2_add(err, t_lo), tail)));
 #else
-    return make_float2(neg_log_grid(ma), neg_log_grid(mb));
+    return make_float2(neg_log_grid_by(ma, load), neg_log_grid_by(mb, load));
 #endif
+}
+
+__device__ __forceinline__ float2 neg_log_grid_x2(uint32_t ma, uint32_t mb)
+{
+    return neg_log_grid_x2_by(ma, mb, [](uint32_t j) { return __ldg(&kNegLogTable[j]); });
 }
 }  // namespace detail
 
