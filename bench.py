@@ -127,7 +127,7 @@ def next_specs():
           lambda r, o, f, s: r.rng_fill_normal_f32_pairs(W.NORMAL_SEED, f, o, s)),
         F("normal_f32_precise", "float32", 4, 0, "fill_kernel<GenNormalF32Precise>", "normal_f32.cu",
           lambda r, o, f, s: r.rng_fill_normal_f32_precise(W.NORMAL_SEED, f, o, s)),
-        F("exponential_f32", "float32", 4, 0, "exp_f32_table_kernel", "exponential.cu",
+        F("exponential_f32", "float32", 4, 0, "neglog_table_kernel<GenExpF32>", "exponential.cu",
           lambda r, o, f, s: r.rng_fill_exponential_f32(W.NORMAL_SEED, f, o, s)),
         F("exponential_f64", "float64", 8, 0, "fill_kernel<GenExpF64>", "exponential.cu",
           lambda r, o, f, s: r.rng_fill_exponential_f64(W.NORMAL_SEED, f, o, s)),
