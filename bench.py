@@ -16,7 +16,8 @@ kernel with the largest share of the step to the measured HBM bandwidth and
 `slowest_fill` gives the slowest call with the pipe that bounds it;
 `next_rows` times the fills beyond the step (paired normals, narrow fills)
 one by one, outside `value`; `configs` times the normals at 2^24 and 2^28
-from first counters 0, 1 and 3; `e2e`
+from first counters 0, 1 and 3; `context_curand` times cuRAND's Philox
+fills of the same size on the same GPU (context only); `e2e`
 repeats the step through the same C ABI with pinned host buffers (inputs
 copied in, every output copied out, inside the timed region);
 `cpu_baseline` times the CPU oracle on a bounded sample.  Under torchrun
@@ -508,6 +509,10 @@ def run_ours(args):
                                     "frac_of_hbm": round(gbs / peak, 3),
                                     "frac_of_write_ceiling": round(gbs / wpeak, 3), "kernel": spec.kernel}
 
+    context = None
+    if not args.no_context and not args.only:
+        context = curand_context(torch, buf8, stream, max(args.steps, 5), n)
+
     configs = None
     if not args.no_configs and not args.only:
         configs = normals_configs(rng, torch, buf8, stream, dev, max(args.steps, 5), base)
@@ -530,7 +535,7 @@ def run_ours(args):
                        "l2": "outputs of 1-2 GiB per fill exceed the 129 MB L2; no flush between steps",
                        "parallelism": f"counter-range shards x{world}"},
             "fills": fills, "write_ceiling": ceiling, "roofline": roofline, "slowest_fill": slow, "next_rows": next_rows,
-            "configs": configs, "e2e": e2e,
+            "configs": configs, "context_curand": context, "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clocks.summary(),
             "cpu_baseline": None if args.no_cpu else cpu_baseline(specs),
@@ -574,6 +579,61 @@ def normals_configs(rng, torch, buf8, stream, dev, reps, base):
                              "l2": "flushed between calls" if n * written <= (256 << 20) else "output > L2"})
     del flush
     return rows
+
+
+def curand_context(torch, buf8, stream, reps, n):
+    """cuRAND's Philox4x32-10 (host API), timed on the same GPU the same way
+    as the fills (median of `reps` event-timed calls after 3 untimed ones) at
+    the same size: context only, as the pages set their A100 fills beside it
+    (tandem-cuda "Performance"); not a target and not part of the step."""
+    lib = None
+    for name in ("libcurand.so", "libcurand.so.10", "/usr/local/cuda/lib64/libcurand.so"):
+        try:
+            lib = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    if lib is None:
+        return {"unavailable": "libcurand not found"}
+    gen = ctypes.c_void_p()
+    philox = 161  # CURAND_RNG_PSEUDO_PHILOX4_32_10
+    if lib.curandCreateGenerator(ctypes.byref(gen), philox) != 0:
+        return {"unavailable": "curandCreateGenerator failed"}
+    sz, vp = ctypes.c_size_t, ctypes.c_void_p
+    lib.curandSetStream.argtypes = [vp, vp]
+    lib.curandSetPseudoRandomGeneratorSeed.argtypes = [vp, ctypes.c_ulonglong]
+    for f in ("curandGenerate", "curandGenerateUniform", "curandGenerateUniformDouble"):
+        getattr(lib, f).argtypes = [vp, vp, sz]
+    lib.curandGenerateNormal.argtypes = [vp, vp, sz, ctypes.c_float, ctypes.c_float]
+    lib.curandGenerateNormalDouble.argtypes = [vp, vp, sz, ctypes.c_double, ctypes.c_double]
+    lib.curandSetStream(gen, vp(stream.cuda_stream or None))
+    lib.curandSetPseudoRandomGeneratorSeed(gen, 7)
+    ptr = vp(buf8.data_ptr())
+    calls = [("u32 (curandGenerate)", 4, lambda: lib.curandGenerate(gen, ptr, n)),
+             ("f32 uniform (curandGenerateUniform)", 4, lambda: lib.curandGenerateUniform(gen, ptr, n)),
+             ("f64 uniform (curandGenerateUniformDouble)", 8, lambda: lib.curandGenerateUniformDouble(gen, ptr, n)),
+             ("normal f32 (curandGenerateNormal)", 4, lambda: lib.curandGenerateNormal(gen, ptr, n, 0.0, 1.0)),
+             ("normal f64 (curandGenerateNormalDouble)", 8,
+              lambda: lib.curandGenerateNormalDouble(gen, ptr, n, 0.0, 1.0))]
+    rows = {}
+    try:
+        for name, size, call in calls:
+            for _ in range(3):
+                if call() != 0:
+                    raise RuntimeError(name)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for a, b in evs:
+                a.record(stream)
+                call()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            rows[name] = {"ms": round(ms, 4), "gib_s_written": round(size * n / (ms / 1e3) / GIB, 1)}
+    except RuntimeError as exc:
+        rows["unavailable"] = f"{exc} failed"
+    finally:
+        lib.curandDestroyGenerator(gen)
+    return {"generator": "cuRAND Philox4x32-10, host API", "elements": n, "rows": rows}
 
 
 def write_ceiling(rng, torch, buf, stream, reps):
@@ -730,6 +790,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the fills beyond the step")
     ap.add_argument("--no-configs", action="store_true", help="skip the normals configuration rows")
+    ap.add_argument("--no-context", action="store_true", help="skip the cuRAND context rows")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("at least 3 warm-up steps")
