@@ -578,28 +578,30 @@ float orc_exponential_f32_own(uint32_t seed, uint32_t counter)
  * READING (the pages' f64 logarithm is not printed; their exponentials need
  * only an own, reproducible log): with V = 2^53 - m (1 - u = V 2^-53 exactly),
  *   V = 2^k M, M in [1, 2), E = 53 - k, so -ln(1 - u) = E ln 2 - ln M;
- *   j = round((M - 1) 256), I_j = 256/(256 + j) rounded to 8 significant
- *   bits times 256 (the reciprocal inv_j = I_j / 256 of the f32 log), and
- *   r = M inv_j - 1 = (V I_j - 2^(k+8)) 2^-(k+8), an exact integer ratio,
- *   |r| < 1.5 2^-8 (Tang 1990, as the f32 log);
- *   log1p(r) = r S(r), S(r) = sum_k (-r)^(k-1) / k for k = 1 .. 8 (Taylor; the
- *   next term is below 2^-62 of the result).  With a = |r| every Horner value
+ *   j = round((M - 1) 2048), halves up; I_j = 2048/(2048 + j) rounded to 11
+ *   significant bits, times 2048 (the reciprocal inv_j = I_j / 2048, I_j in
+ *   [1024, 2048]); r = M inv_j - 1, |r| < 1.5 2^-11 (Tang 1990's table
+ *   reduction).  With W = V 2^(62 - k) (M at scale 2^62), W I_j = (1 + r)
+ *   2^73, so W I_j modulo 2^64 is r 2^73 in two's complement, exactly
+ *   (|r| 2^73 < 2^63);
+ *   log1p(r) = r S(r), S(r) = sum_k (-r)^(k-1) / k for k = 1 .. 6 (Taylor; the
+ *   next term is below 2^-65 of the result).  With a = |r| every Horner value
  *   S_k = 1/k + (-r) S_(k+1) is positive: S_k = 1/k + a S_(k+1) for r < 0 and
- *   1/k - a S_(k+1) for r >= 0.  S_8 .. S_6 in 32-bit fixed point (scale
- *   2^31; those steps need only 2^-26), S_5 .. S_1 in 64-bit fixed point
- *   (scale 2^62), each product's high part floored; a S exact in 128 bits
- *   (scale 2^132);
- *   -ln(1 - u) = E ln 2 + ln inv_j -+ a S (minus for r >= 0), with E ln2 +
+ *   1/k - a S_(k+1) for r >= 0.  Each product is floored to the scale of the
+ *   value it feeds: S_6 .. S_4 at 2^33 and S_3 at 2^64 take a floored to
+ *   2^-42 (a 32-bit number), S_2 at 2^64 and S_1 at 2^63 take a itself; a S_1
+ *   exact in 128 bits (scale 2^136);
+ *   -ln(1 - u) = E ln 2 + ln inv_j -+ a S_1 (minus for r >= 0), with E ln 2 +
  *   ln inv_j at scale 2^96 (ln 2 and ln inv_j each rounded once to the
- *   nearest multiple of 2^-96) and a S floored to it; where E ln 2 + ln inv_j
- *   is exactly 0 (E = 1, inv_j = 1/2, so r < 0) the value is a S itself, at
- *   scale 2^132;
+ *   nearest multiple of 2^-96) and a S_1 floored to it; where E ln 2 + ln inv_j
+ *   is exactly 0 (E = 1, inv_j = 1/2, so r < 0) the value is a S_1 itself, at
+ *   scale 2^136;
  *   the positive fixed-point value rounded once to binary64, to nearest even.
- * Within 0.5005 ulp of the exact value on the inputs tried. */
-static int32_t nl64_i[257];
-static __int128 nl64_lninv[257], nl64_ln2;
-static uint64_t nl64_d64[6]; /* 1/k at 2^62, k = 1 .. 5 */
-static uint32_t nl64_d32[9]; /* 1/k at 2^31, k = 6 .. 8 */
+ * Within 0.5007 ulp of the exact value on the inputs tried. */
+#define NL64_BINS 2048
+static int32_t nl64_i[NL64_BINS + 1];
+static __int128 nl64_lninv[NL64_BINS + 1], nl64_ln2;
+static uint64_t nl64_c[7]; /* 1/k at the scale of S_k: 2^63 (k = 1), 2^64 (k = 2, 3), 2^33 (k = 4 .. 6) */
 static int nl64_ready;
 
 static __int128 nl64_round96(quad v) { return (__int128)Q_RINT(v * (quad)79228162514264337593543950336.0); } /* 2^96 */
@@ -607,13 +609,14 @@ static __int128 nl64_round96(quad v) { return (__int128)Q_RINT(v * (quad)7922816
 static void nl64_init(void)
 {
     if (nl64_ready) return;
-    for (int j = 0; j <= 256; ++j) {
-        nl64_i[j] = (int32_t)(round_to_bits(256.0 / (256.0 + j), 8) * 256.0);
-        nl64_lninv[j] = nl64_round96(Q_LOG((quad)nl64_i[j] / 256));
+    for (int j = 0; j <= NL64_BINS; ++j) {
+        nl64_i[j] = (int32_t)(round_to_bits(2048.0 / (2048.0 + j), 11) * 2048.0);
+        nl64_lninv[j] = nl64_round96(Q_LOG((quad)nl64_i[j] / 2048));
     }
     nl64_ln2 = nl64_round96(Q_LOG((quad)2));
-    for (int k = 1; k <= 5; ++k) nl64_d64[k] = (uint64_t)Q_RINT((quad)4611686018427387904.0 / k); /* 2^62 / k */
-    for (int k = 6; k <= 8; ++k) nl64_d32[k] = (uint32_t)Q_RINT((quad)2147483648.0 / k);          /* 2^31 / k */
+    static const int scale[7] = {0, 63, 64, 64, 33, 33, 33}; /* of S_k */
+    for (int k = 1; k <= 6; ++k) /* 1/k at 2^scale, to nearest (no k here gives a half) */
+        nl64_c[k] = (uint64_t)((((unsigned __int128)1 << scale[k]) + (unsigned)k / 2) / (unsigned)k);
     nl64_ready = 1;
 }
 
@@ -642,26 +645,27 @@ double orc_neglog64(uint64_t m) /* m < 2^53 */
     uint64_t V = (1ull << 53) - m;
     int k = 63 - __builtin_clzll(V);
     int E = 53 - k;
-    uint64_t Vn = V << (63 - k);
-    uint32_t j = (uint32_t)(((Vn - (1ull << 63)) + (1ull << 54)) >> 55);
-    int64_t R = (int64_t)(V * (uint64_t)nl64_i[j]) - (int64_t)(1ull << (k + 8));
-    int up = R < 0; /* -r > 0: every Horner term adds */
-    uint64_t a = (uint64_t)(up ? -R : R) << (62 - k); /* |r| 2^70, exact */
-    uint32_t a32 = (uint32_t)(a >> 32);             /* |r| 2^38 */
-    uint32_t S32 = nl64_d32[8];
-    for (int t = 7; t >= 6; --t) {
-        uint32_t p = (uint32_t)(((uint64_t)a32 * S32) >> 38); /* floor(a S 2^-38) at 2^31 */
-        S32 = up ? nl64_d32[t] + p : nl64_d32[t] - p;
+    uint64_t W = V << (62 - k);                                          /* M 2^62 */
+    uint32_t j = (uint32_t)(((W - (1ull << 62)) + (1ull << 50)) >> 51); /* round((M - 1) 2048) */
+    uint64_t P = W * (uint64_t)nl64_i[j]; /* (1 + r) 2^73 modulo 2^64: r 2^73 */
+    int up = (int)(P >> 63);             /* r < 0, -r > 0: every Horner term adds */
+    uint64_t a = up ? 0 - P : P;         /* |r| 2^73, exact */
+    uint64_t a42 = a >> 31;              /* |r| 2^42, floored; below 2^32 */
+    uint64_t S = nl64_c[6];              /* S_6 at 2^33 */
+    for (int t = 5; t >= 4; --t) {
+        uint64_t p = (a42 * S) >> 42; /* floor(a S_(t+1)) at 2^33 */
+        S = up ? nl64_c[t] + p : nl64_c[t] - p;
     }
-    uint64_t S = (uint64_t)S32 << 31; /* to 2^62 */
-    for (int t = 5; t >= 1; --t) {
-        uint64_t p = (uint64_t)(((unsigned __int128)a * S) >> 70); /* floor(a S 2^-70) at 2^62 */
-        S = up ? nl64_d64[t] + p : nl64_d64[t] - p;
-    }
-    unsigned __int128 Pm = (unsigned __int128)a * S; /* |log1p(r)| 2^132, exact */
-    if (E == 1 && nl64_i[j] == 128) return nl64_to_double(Pm, 132);
+    uint64_t p3 = (a42 * S) >> 11; /* floor(a S_4) at 2^64 */
+    S = up ? nl64_c[3] + p3 : nl64_c[3] - p3;
+    uint64_t p2 = (uint64_t)(((unsigned __int128)a * S) >> 73); /* floor(a S_3) at 2^64 */
+    S = up ? nl64_c[2] + p2 : nl64_c[2] - p2;
+    uint64_t p1 = (uint64_t)(((unsigned __int128)a * S) >> 74); /* floor(a S_2) at 2^63 */
+    S = up ? nl64_c[1] + p1 : nl64_c[1] - p1;
+    unsigned __int128 Pm = (unsigned __int128)a * S; /* |log1p(r)| 2^136, exact */
+    if (E == 1 && nl64_i[j] == 1024) return nl64_to_double(Pm, 136);
     __int128 T = (__int128)E * nl64_ln2 + nl64_lninv[j];
-    __int128 y = up ? T + (__int128)(Pm >> 36) : T - (__int128)(Pm >> 36);
+    __int128 y = up ? T + (__int128)(Pm >> 40) : T - (__int128)(Pm >> 40);
     return nl64_to_double((unsigned __int128)y, 96);
 }
 
@@ -672,19 +676,17 @@ double orc_exponential_f64(uint32_t seed, uint32_t counter)
     return orc_neglog64(orc_draw64(seed, counter) >> 11);
 }
 
-void orc_neglog64_table(int32_t *inv256, int64_t *lninv_hi, uint64_t *lninv_lo, int64_t *ln2, int64_t *coef)
+void orc_neglog64_table(int32_t *inv2048, int64_t *lninv_hi, uint64_t *lninv_lo, int64_t *ln2, uint64_t *coef)
 {
     nl64_init();
-    for (int j = 0; j <= 256; ++j) {
-        inv256[j] = nl64_i[j];
+    for (int j = 0; j <= NL64_BINS; ++j) {
+        inv2048[j] = nl64_i[j];
         lninv_hi[j] = (int64_t)(nl64_lninv[j] >> 64);
         lninv_lo[j] = (uint64_t)nl64_lninv[j];
     }
     ln2[0] = (int64_t)(nl64_ln2 >> 64);
     ln2[1] = (int64_t)(uint64_t)nl64_ln2;
-    coef[0] = 0;
-    for (int k = 1; k <= 5; ++k) coef[k] = (int64_t)nl64_d64[k];
-    for (int k = 6; k <= 8; ++k) coef[k] = (int64_t)nl64_d32[k];
+    for (int k = 0; k <= 6; ++k) coef[k] = nl64_c[k];
 }
 
 /* ------------------------------------------------------------------------ */

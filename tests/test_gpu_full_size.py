@@ -108,7 +108,7 @@ def test_full_size_exponential_f64_within_its_bound(rng, torch, orc, sample):
     """The GPU's f64 exponential against a plain reference that shares nothing
     with the own fixed-point logarithm: -log1p(-u) of u = (draw64 >> 11) 2^-53
     in numpy's longdouble (x87 extended on x86-64, binary128 on aarch64),
-    within the stated 0.5025 ulp at every sampled element of the 2^28 fill."""
+    within the stated 0.501 ulp at every sampled element of the 2^28 fill."""
     if np.finfo(np.longdouble).nmant < 63:
         pytest.skip("needs a longdouble of at least 64 significand bits")
     out = torch.empty(N, dtype=torch.float64, device="cuda")
@@ -119,7 +119,7 @@ def test_full_size_exponential_f64_within_its_bound(rng, torch, orc, sample):
     zero = m == 0
     assert np.all(y[zero] == 0) and not np.any(np.signbit(y[zero]))
     err = np.abs(y[~zero].astype(np.longdouble) - ref[~zero]) / np.spacing(ref[~zero].astype(np.float64))
-    assert float(err.max()) <= 0.5025, float(err.max())
+    assert float(err.max()) <= 0.501, float(err.max())
     del out
     torch.cuda.empty_cache()
 

@@ -47,7 +47,7 @@ def test_f64_log_table_equals_the_oracle(orc):
     text = open(os.path.join(CSRC, "neglog64_table.inc")).read()
     rows = re.findall(r"\{0x([0-9a-f]+)ull, 0x([0-9a-f]+)ull\}", text)
     inv, lninv, ln2, coef = orc.neglog64_table()
-    assert len(rows) == 257
+    assert len(rows) == 2049
     for j, (lo, packed) in enumerate(rows):
         lo, packed = int(lo, 16), int(packed, 16)
         hi = packed & ((1 << 48) - 1)
@@ -57,5 +57,5 @@ def test_f64_log_table_equals_the_oracle(orc):
     lo = int(re.search(r"kNegLog64Ln2Lo = 0x([0-9a-f]+)ull", text).group(1), 16)
     hi = int(re.search(r"kNegLog64Ln2Hi = (-?\d+)ll", text).group(1))
     assert (hi << 64) + lo == ln2
-    for k in range(1, 9):
+    for k in range(1, 7):
         assert int(re.search(rf"kNegLog64D{k} = (\d+)u", text).group(1)) == coef[k], k
