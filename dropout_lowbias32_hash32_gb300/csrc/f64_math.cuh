@@ -78,27 +78,27 @@ __device__ __forceinline__ double zlog(double x)
 #include "neglog64_table.inc"
 
 // y 2^-scale for an integer 2^64 <= y < 2^128 (on both paths of neglog64 y is
-// at least 2^83), rounded to the nearest binary64, ties to even: y is shifted
-// left until its leading one is bit 127 (z places), the significand is then
-// bits 127 .. 75, the rounding bit bit 74 and the sticky bits 73 .. 0; the
-// value is mant 2^(75 - z - scale).  The same result as rounding y 2^-scale
-// directly, on 64-bit halves only.
+// at least 2^83), rounded to the nearest binary64, ties to even.  y is shifted
+// left until its leading one is bit 127 (z places); the high word H then holds
+// the significand (bits 63 .. 11), the rounding bit (bit 10) and the top of
+// the sticky bits, and whether any bit of the low word is set is folded into
+// bit 0 of H, below the rounding bit, which keeps both the rounding and the
+// tie decision.  One round-to-nearest conversion of that 64-bit integer (IEEE,
+// on the otherwise idle FP64 pipe) rounds it to 53 bits; the exact power of
+// two 2^(64 - z - scale) is then added to the exponent field.  The same result
+// as rounding y 2^-scale directly; the conversion replaced seven ALU
+// instructions of an integer rounding (1.852 against 1.930 ms per 2^28 fill).
 __device__ __forceinline__ double fixed_to_double(unsigned __int128 y, int scale)
 {
     const unsigned long long hi = static_cast<unsigned long long>(y >> 64);
     const unsigned long long lo = static_cast<unsigned long long>(y);
-    const int z = __clzll(static_cast<long long>(hi));           // 0 .. 63: hi != 0
+    const int z = __clzll(static_cast<long long>(hi));                // 0 .. 63: hi != 0
     const unsigned long long H = (hi << z) | ((lo >> 1) >> (63 - z));  // (hi:lo) << z, high word
     const unsigned long long L = lo << z;
-    unsigned long long mant = H >> 11;
-    const unsigned long long round = (H >> 10) & 1ull;
-    const unsigned long long sticky = ((H & 0x3FFull) | L) != 0ull;
-    mant += round & (sticky | (mant & 1ull));
-    // mant in [2^52, 2^53]: biased exponent 1023 + 52 + 75 - z - scale,
-    // written one lower because the significand's leading one (or a rounding
-    // carry to 2^53) adds one to the field
-    const long long e = 1022 + 52 + 75 - z - scale;
-    return __longlong_as_double(static_cast<long long>((static_cast<unsigned long long>(e) << 52) + mant));
+    const double d = __ull2double_rn(H | static_cast<unsigned long long>(L != 0ull));  // in [2^63, 2^64]
+    const long long adj = static_cast<long long>(64 - z - scale);
+    return __longlong_as_double(static_cast<long long>(static_cast<unsigned long long>(__double_as_longlong(d)) +
+                                                       (static_cast<unsigned long long>(adj) << 52)));
 }
 
 // -ln(1 - m 2^-53) for m < 2^53 in integer arithmetic only (tandem-sycl
