@@ -78,7 +78,7 @@ __device__ __forceinline__ double zlog(double x)
 #include "neglog64_table.inc"
 
 // y 2^-scale for an integer 2^64 <= y < 2^128 (on both paths of neglog64 y is
-// at least 2^83), rounded to the nearest binary64, ties to even.  y is shifted
+// at least 2^84), rounded to the nearest binary64, ties to even.  y is shifted
 // left until its leading one is bit 127 (z places); the high word H then holds
 // the significand (bits 63 .. 11), the rounding bit (bit 10) and the top of
 // the sticky bits, and whether any bit of the low word is set is folded into
@@ -101,55 +101,60 @@ __device__ __forceinline__ double fixed_to_double(unsigned __int128 y, int scale
                                                        (static_cast<unsigned long long>(adj) << 52)));
 }
 
+// a S_1 of log1p's series at scale 2^137 for a at scale 2^74: S = sum of
+// (-a)^(k-1)/k to k = 6 by Horner, or with every term added (kAdd, the series
+// of -ln(1 - u) in u), each product floored: S_5, S_4 in 32 bits at 2^33 from a
+// at 2^42, S_3 at 2^64 from their 32 x 32 product, S_2 at 2^64 and S_1 at 2^63
+// from a itself; a S_1 exact in 128 bits.
+template <bool kAdd>
+__device__ __forceinline__ unsigned __int128 neglog64_series(unsigned long long a)
+{
+    const unsigned a42 = static_cast<unsigned>(a >> 32);  // a 2^42, below 2^32
+    unsigned p32 = __umulhi(a42, kNegLog64D6) >> 10;      // floor(a S 2^-42) at 2^33
+    unsigned S32 = kAdd ? kNegLog64D5 + p32 : kNegLog64D5 - p32;
+    p32 = __umulhi(a42, S32) >> 10;
+    S32 = kAdd ? kNegLog64D4 + p32 : kNegLog64D4 - p32;
+    unsigned long long p = (static_cast<unsigned long long>(a42) * S32) >> 11;  // at 2^64
+    unsigned long long S = kAdd ? kNegLog64D3 + p : kNegLog64D3 - p;
+    p = __umul64hi(a, S) >> 10;  // floor(a S 2^-74) at 2^64
+    S = kAdd ? kNegLog64D2 + p : kNegLog64D2 - p;
+    p = __umul64hi(a, S) >> 11;  // at 2^63
+    S = kAdd ? kNegLog64D1 + p : kNegLog64D1 - p;
+    return static_cast<unsigned __int128>(a) * S;
+}
+
 // -ln(1 - m 2^-53) for m < 2^53 in integer arithmetic only (tandem-sycl
 // "Design", Exponentials: an own reproducible logarithm).  V = 2^53 - m = 2^k M,
-// E = 53 - k; bin j = round((M - 1) 2048) with I_j = 2048 inv_j; with W = M
-// 2^62, W I_j = (1 + r) 2^73, so the 64-bit product read as signed is r 2^73
-// exactly (|r| < 1.5 2^-11); log1p(r) = r S(r), S = sum (-r)^(k-1)/k to k = 6
-// by Horner on a = |r| (every Horner value positive: S_k = 1/k + a S_(k+1) for
-// r < 0, 1/k - a S_(k+1) otherwise), products floored: S_5, S_4 in 32 bits at
-// 2^33 from a at 2^42, S_3 at 2^64 from their 32 x 32 product, S_2 at 2^64 and
-// S_1 at 2^63 from a at 2^73; a S_1 exact in 128 bits (scale 2^136);
-// -ln(1 - u) = E ln 2 + ln inv_j -+ a S_1 at scale 2^96, or a S_1 itself where
-// E ln 2 + ln inv_j is exactly 0 (E = 1, inv_j = 1/2); rounded once to
-// binary64.  Within 0.5007 ulp.
+// E = 53 - k; bin j = floor((M - 1) 2048) with I_j = 4096 inv_j, the reciprocal
+// rounded up, so r = M inv_j - 1 is in [0, 1.5 2^-11); with W = M 2^62,
+// W I_j = (1 + r) 2^74, so the 64-bit product is r 2^74 exactly.  log1p(r) =
+// r S(r) by neglog64_series, all its Horner steps subtractions; -ln(1 - u) =
+// E ln 2 + ln inv_j - r S at scale 2^96, rounded once to binary64.  For m <=
+// 2^41 (u <= 2^-12, about one draw in 4096), where that sum would cancel, the
+// value is u S(-u) from the same series with every term added, at 2^137.
+// Within 0.5007 ulp.
 __device__ __forceinline__ double neglog64(unsigned long long m)
 {
-    if (m == 0) return 0.0;
+    if (m <= (1ull << 41)) {
+        if (m == 0) return 0.0;
+        return fixed_to_double(neglog64_series<true>(m << 21), 137);  // u 2^74
+    }
     const unsigned long long V = (1ull << 53) - m;
     const int k = 63 - __clzll(static_cast<long long>(V));
     const int E = 53 - k;
     const unsigned long long W = V << (62 - k);  // M 2^62
-    const unsigned j = static_cast<unsigned>(((W - (1ull << 62)) + (1ull << 50)) >> 51);
+    const unsigned j = static_cast<unsigned>((W - (1ull << 62)) >> 51);
     const ulonglong2 row = __ldg(&kNegLog64Table[j]);
     const unsigned inv = static_cast<unsigned>(row.y >> 48);
-    const unsigned long long P = W * inv;  // (1 + r) 2^73 modulo 2^64: r 2^73
-    const bool up = static_cast<long long>(P) < 0;  // -r > 0: every Horner term adds
-    const unsigned long long a = up ? 0ull - P : P;  // |r| 2^73
-    const unsigned a42 = static_cast<unsigned>(a >> 31);  // |r| 2^42, below 2^32
-    unsigned p32 = __umulhi(a42, kNegLog64D6) >> 10;  // floor(a S 2^-42) at 2^33
-    unsigned S32 = up ? kNegLog64D5 + p32 : kNegLog64D5 - p32;
-    p32 = __umulhi(a42, S32) >> 10;
-    S32 = up ? kNegLog64D4 + p32 : kNegLog64D4 - p32;
-    unsigned long long p = (static_cast<unsigned long long>(a42) * S32) >> 11;  // at 2^64
-    unsigned long long S = up ? kNegLog64D3 + p : kNegLog64D3 - p;
-    p = __umul64hi(a, S) >> 9;  // floor(a S 2^-73) at 2^64
-    S = up ? kNegLog64D2 + p : kNegLog64D2 - p;
-    p = __umul64hi(a, S) >> 10;  // at 2^63
-    S = up ? kNegLog64D1 + p : kNegLog64D1 - p;
-    const unsigned __int128 Pm = static_cast<unsigned __int128>(a) * S;  // |log1p(r)| 2^136
+    const unsigned __int128 Pm = neglog64_series<false>(W * inv);  // log1p(r) 2^137
     const long long lninv_hi = static_cast<long long>(row.y << 16) >> 16;  // the signed 48-bit field
     // two's complement of lninv_hi 2^64 + low: the high word's 64-bit pattern above the low word
     const __int128 lninv = static_cast<__int128>(
         (static_cast<unsigned __int128>(static_cast<unsigned long long>(lninv_hi)) << 64) | row.x);
     const __int128 ln2 = static_cast<__int128>(
         (static_cast<unsigned __int128>(static_cast<unsigned long long>(kNegLog64Ln2Hi)) << 64) | kNegLog64Ln2Lo);
-    // a S_1 itself (scale 2^136) where E ln 2 + ln inv_j is exactly 0, else the sum at 2^96
-    const bool exact_small = E == 1 && inv == 1024u;
     const __int128 T = static_cast<__int128>(E) * ln2 + lninv;
-    const __int128 q = static_cast<__int128>(Pm >> 40);
-    const unsigned __int128 y = exact_small ? Pm : static_cast<unsigned __int128>(up ? T + q : T - q);
-    return fixed_to_double(y, exact_small ? 136 : 96);
+    return fixed_to_double(static_cast<unsigned __int128>(T - static_cast<__int128>(Pm >> 41)), 96);
 }
 
 }  // namespace rngk

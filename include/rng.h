@@ -222,12 +222,14 @@ rng_status rng_fill_exponential_f32(uint32_t seed, uint32_t first_counter, size_
 
 /* out[i] = -ln(1 - u), u = (D64(seed, c_i) >> 11) 2^-53, by neglog64: a
  * fixed-point logarithm in 32-, 64- and 128-bit integer arithmetic with no
- * FP64 operation.  1 - u = V 2^-53 with the integer V = 2^53 - m is reduced
- * exactly by 11-bit reciprocals (a 2049-row table), log1p of the reduced
- * argument is a Horner series to r^6 in fixed point, the exponent and table
- * terms are added at scale 2^96, and the sum is rounded once to binary64.
- * Within 0.5007 ulp of -ln(1 - u), reproducible bit for bit, in
- * [0, 53 ln 2]; +0 at u = 0.  Bound by the integer pipes on GB300. */
+ * FP64 arithmetic (one u64 -> f64 conversion rounds the result).  1 - u =
+ * V 2^-53 with the integer V = 2^53 - m is reduced exactly by 2048 one-sided
+ * reciprocals (r in [0, 1.5 2^-11)), log1p of the reduced argument is a
+ * Horner series to r^5 in fixed point, the exponent and table terms are added
+ * at scale 2^96, and the sum is rounded once to binary64; below u = 2^-12 the
+ * value is the series in u itself.  Within 0.5007 ulp of -ln(1 - u),
+ * reproducible bit for bit, in [0, 53 ln 2]; +0 at u = 0.  Bound by the
+ * integer pipes on GB300. */
 rng_status rng_fill_exponential_f64(uint32_t seed, uint32_t first_counter, size_t n, double *out,
                                     void *stream);
 

@@ -362,11 +362,11 @@ class Oracle:
         return out
 
     def neglog64_table(self):
-        """I_j (2049), ln inv_j at 2^96 as Python ints (2049), ln 2 at 2^96, and the
+        """I_j (2048), ln inv_j at 2^96 as Python ints (2048), ln 2 at 2^96, and the
         Horner constants 1/k (index k = 1 .. 6): 1 at 2^63, 1/2 and 1/3 at 2^64,
         1/4 .. 1/6 at 2^33."""
-        inv = np.empty(2049, np.int32)
-        hi, lo = np.empty(2049, np.int64), np.empty(2049, np.uint64)
+        inv = np.empty(2048, np.int32)
+        hi, lo = np.empty(2048, np.int64), np.empty(2048, np.uint64)
         ln2, coef = np.empty(2, np.int64), np.empty(7, np.uint64)
         self.lib.orc_neglog64_table(_ptr(inv), _ptr(hi), _ptr(lo), _ptr(ln2), _ptr(coef))
         lninv = [(int(h) << 64) + int(l) for h, l in zip(hi, lo)]

@@ -578,29 +578,29 @@ float orc_exponential_f32_own(uint32_t seed, uint32_t counter)
  * READING (the pages' f64 logarithm is not printed; their exponentials need
  * only an own, reproducible log): with V = 2^53 - m (1 - u = V 2^-53 exactly),
  *   V = 2^k M, M in [1, 2), E = 53 - k, so -ln(1 - u) = E ln 2 - ln M;
- *   j = round((M - 1) 2048), halves up; I_j = 2048/(2048 + j) rounded to 11
- *   significant bits, times 2048 (the reciprocal inv_j = I_j / 2048, I_j in
- *   [1024, 2048]); r = M inv_j - 1, |r| < 1.5 2^-11 (Tang 1990's table
- *   reduction).  With W = V 2^(62 - k) (M at scale 2^62), W I_j = (1 + r)
- *   2^73, so W I_j modulo 2^64 is r 2^73 in two's complement, exactly
- *   (|r| 2^73 < 2^63);
- *   log1p(r) = r S(r), S(r) = sum_k (-r)^(k-1) / k for k = 1 .. 6 (Taylor; the
- *   next term is below 2^-65 of the result).  With a = |r| every Horner value
- *   S_k = 1/k + (-r) S_(k+1) is positive: S_k = 1/k + a S_(k+1) for r < 0 and
- *   1/k - a S_(k+1) for r >= 0.  Each product is floored to the scale of the
- *   value it feeds: S_6 .. S_4 at 2^33 and S_3 at 2^64 take a floored to
- *   2^-42 (a 32-bit number), S_2 at 2^64 and S_1 at 2^63 take a itself; a S_1
- *   exact in 128 bits (scale 2^136);
- *   -ln(1 - u) = E ln 2 + ln inv_j -+ a S_1 (minus for r >= 0), with E ln 2 +
- *   ln inv_j at scale 2^96 (ln 2 and ln inv_j each rounded once to the
- *   nearest multiple of 2^-96) and a S_1 floored to it; where E ln 2 + ln inv_j
- *   is exactly 0 (E = 1, inv_j = 1/2, so r < 0) the value is a S_1 itself, at
- *   scale 2^136;
+ *   j = floor((M - 1) 2048), and I_j = 2^23/(2048 + j) rounded up to an
+ *   integer (12 significant bits, I_j in [2049, 4096]): the reciprocal
+ *   inv_j = I_j / 4096 >= 1/(1 + j/2048), so r = M inv_j - 1 is never negative
+ *   and r < 1.5 2^-11 (Tang 1990's table reduction, one-sided).  With
+ *   W = V 2^(62 - k) (M at scale 2^62), W I_j = (1 + r) 2^74, so W I_j modulo
+ *   2^64 is r 2^74 exactly (r 2^74 < 1.5 2^63);
+ *   log1p(r) = r S(r), S(r) = sum_k (-r)^(k-1) / k for k = 1 .. 6 (Taylor;
+ *   the next term is below 2^-65 of the result), by Horner on a = r: every
+ *   value S_k = 1/k - a S_(k+1) is positive.  Each product is floored to the
+ *   scale of the value it feeds: S_5 and S_4 at 2^33 and S_3 at 2^64 take a
+ *   floored to 2^-42 (a 32-bit number), S_2 at 2^64 and S_1 at 2^63 take a
+ *   itself; a S_1 exact in 128 bits (scale 2^137);
+ *   -ln(1 - u) = E ln 2 + ln inv_j - a S_1, with E ln 2 + ln inv_j at scale
+ *   2^96 (ln 2 and ln inv_j each rounded once to the nearest multiple of
+ *   2^-96) and a S_1 floored to it.
+ *   For m <= 2^41 (u <= 2^-12, where E ln 2 + ln inv_j would cancel against
+ *   log1p(r)) the value is the series itself: -ln(1 - u) = u S(-u) with the
+ *   same Horner steps on a = u (every term added), a S_1 at scale 2^137;
  *   the positive fixed-point value rounded once to binary64, to nearest even.
  * Within 0.5007 ulp of the exact value on the inputs tried. */
 #define NL64_BINS 2048
-static int32_t nl64_i[NL64_BINS + 1];
-static __int128 nl64_lninv[NL64_BINS + 1], nl64_ln2;
+static int32_t nl64_i[NL64_BINS];
+static __int128 nl64_lninv[NL64_BINS], nl64_ln2;
 static uint64_t nl64_c[7]; /* 1/k at the scale of S_k: 2^63 (k = 1), 2^64 (k = 2, 3), 2^33 (k = 4 .. 6) */
 static int nl64_ready;
 
@@ -609,9 +609,10 @@ static __int128 nl64_round96(quad v) { return (__int128)Q_RINT(v * (quad)7922816
 static void nl64_init(void)
 {
     if (nl64_ready) return;
-    for (int j = 0; j <= NL64_BINS; ++j) {
-        nl64_i[j] = (int32_t)(round_to_bits(2048.0 / (2048.0 + j), 11) * 2048.0);
-        nl64_lninv[j] = nl64_round96(Q_LOG((quad)nl64_i[j] / 2048));
+    for (int j = 0; j < NL64_BINS; ++j) {
+        uint32_t d = 2048u + (uint32_t)j;
+        nl64_i[j] = (int32_t)(((1u << 23) + d - 1u) / d); /* ceil(2^23 / (2048 + j)) */
+        nl64_lninv[j] = nl64_round96(Q_LOG((quad)nl64_i[j] / 4096));
     }
     nl64_ln2 = nl64_round96(Q_LOG((quad)2));
     static const int scale[7] = {0, 63, 64, 64, 33, 33, 33}; /* of S_k */
@@ -638,34 +639,40 @@ static double nl64_to_double(unsigned __int128 y, int scale)
     return ldexp((double)mant, shift - scale); /* mant <= 2^53: exact in binary64 */
 }
 
+/* a S_1 of the series above at scale 2^137 for a at scale 2^74; add = 1 takes
+ * every Horner term with a plus sign (S(-a), for the small-u series), add = 0
+ * with alternating signs (S(a)) */
+static unsigned __int128 nl64_series(uint64_t a, int add)
+{
+    uint64_t a42 = a >> 32; /* a 2^42, floored; below 2^32 */
+    uint64_t S = nl64_c[6]; /* S_6 at 2^33 */
+    for (int t = 5; t >= 4; --t) {
+        uint64_t p = (a42 * S) >> 42; /* floor(a S_(t+1)) at 2^33 */
+        S = add ? nl64_c[t] + p : nl64_c[t] - p;
+    }
+    uint64_t p3 = (a42 * S) >> 11; /* floor(a S_4) at 2^64 */
+    S = add ? nl64_c[3] + p3 : nl64_c[3] - p3;
+    uint64_t p2 = (uint64_t)(((unsigned __int128)a * S) >> 74); /* floor(a S_3) at 2^64 */
+    S = add ? nl64_c[2] + p2 : nl64_c[2] - p2;
+    uint64_t p1 = (uint64_t)(((unsigned __int128)a * S) >> 75); /* floor(a S_2) at 2^63 */
+    S = add ? nl64_c[1] + p1 : nl64_c[1] - p1;
+    return (unsigned __int128)a * S; /* a S_1 at 2^137, exact */
+}
+
 double orc_neglog64(uint64_t m) /* m < 2^53 */
 {
     nl64_init();
     if (m == 0) return 0.0;
+    if (m <= (1ull << 41)) return nl64_to_double(nl64_series(m << 21, 1), 137); /* u 2^74 */
     uint64_t V = (1ull << 53) - m;
     int k = 63 - __builtin_clzll(V);
     int E = 53 - k;
-    uint64_t W = V << (62 - k);                                          /* M 2^62 */
-    uint32_t j = (uint32_t)(((W - (1ull << 62)) + (1ull << 50)) >> 51); /* round((M - 1) 2048) */
-    uint64_t P = W * (uint64_t)nl64_i[j]; /* (1 + r) 2^73 modulo 2^64: r 2^73 */
-    int up = (int)(P >> 63);             /* r < 0, -r > 0: every Horner term adds */
-    uint64_t a = up ? 0 - P : P;         /* |r| 2^73, exact */
-    uint64_t a42 = a >> 31;              /* |r| 2^42, floored; below 2^32 */
-    uint64_t S = nl64_c[6];              /* S_6 at 2^33 */
-    for (int t = 5; t >= 4; --t) {
-        uint64_t p = (a42 * S) >> 42; /* floor(a S_(t+1)) at 2^33 */
-        S = up ? nl64_c[t] + p : nl64_c[t] - p;
-    }
-    uint64_t p3 = (a42 * S) >> 11; /* floor(a S_4) at 2^64 */
-    S = up ? nl64_c[3] + p3 : nl64_c[3] - p3;
-    uint64_t p2 = (uint64_t)(((unsigned __int128)a * S) >> 73); /* floor(a S_3) at 2^64 */
-    S = up ? nl64_c[2] + p2 : nl64_c[2] - p2;
-    uint64_t p1 = (uint64_t)(((unsigned __int128)a * S) >> 74); /* floor(a S_2) at 2^63 */
-    S = up ? nl64_c[1] + p1 : nl64_c[1] - p1;
-    unsigned __int128 Pm = (unsigned __int128)a * S; /* |log1p(r)| 2^136, exact */
-    if (E == 1 && nl64_i[j] == 1024) return nl64_to_double(Pm, 136);
+    uint64_t W = V << (62 - k);                     /* M 2^62 */
+    uint32_t j = (uint32_t)((W - (1ull << 62)) >> 51); /* floor((M - 1) 2048) */
+    uint64_t a = W * (uint64_t)nl64_i[j];           /* (1 + r) 2^74 modulo 2^64: r 2^74 */
+    unsigned __int128 Pm = nl64_series(a, 0);       /* log1p(r) 2^137 */
     __int128 T = (__int128)E * nl64_ln2 + nl64_lninv[j];
-    __int128 y = up ? T + (__int128)(Pm >> 40) : T - (__int128)(Pm >> 40);
+    __int128 y = T - (__int128)(Pm >> 41);
     return nl64_to_double((unsigned __int128)y, 96);
 }
 
@@ -676,11 +683,11 @@ double orc_exponential_f64(uint32_t seed, uint32_t counter)
     return orc_neglog64(orc_draw64(seed, counter) >> 11);
 }
 
-void orc_neglog64_table(int32_t *inv2048, int64_t *lninv_hi, uint64_t *lninv_lo, int64_t *ln2, uint64_t *coef)
+void orc_neglog64_table(int32_t *inv4096, int64_t *lninv_hi, uint64_t *lninv_lo, int64_t *ln2, uint64_t *coef)
 {
     nl64_init();
-    for (int j = 0; j <= NL64_BINS; ++j) {
-        inv2048[j] = nl64_i[j];
+    for (int j = 0; j < NL64_BINS; ++j) {
+        inv4096[j] = nl64_i[j];
         lninv_hi[j] = (int64_t)(nl64_lninv[j] >> 64);
         lninv_lo[j] = (uint64_t)nl64_lninv[j];
     }

@@ -519,13 +519,15 @@ def pin_randn_precise(orc):
 
 
 def _neglog64_sample():
-    """53-bit inputs: edge values, every bin edge of the log's table at the two
-    largest exponents, and random values of every bit length."""
+    """53-bit inputs: edge values, both sides of the small-u boundary m = 2^41,
+    every bin edge of the log's table at the two largest exponents, and random
+    values of every bit length."""
     g = np.random.default_rng(9)
     ms = [0, 1, 2, 3, (1 << 52) - 1, 1 << 52, (1 << 52) + 1, (1 << 53) - 2, (1 << 53) - 1]
-    for k in (52, 51):  # V = 2^53 - m in [2^k, 2^(k+1)): bin j starts at M = 1 + (j - 1/2)/2048
-        for j in range(1, 2049):
-            edge = (1 << 53) - (((2 * j - 1) << k) // 4096 + (1 << k))
+    ms += [(1 << 41) + d for d in range(-3, 4)]
+    for k in (52, 51):  # V = 2^53 - m in [2^k, 2^(k+1)): bin j starts at M = 1 + j/2048
+        for j in range(1, 2048):
+            edge = (1 << 53) - ((j << k) >> 11) - (1 << k)
             ms += [edge + d for d in (-1, 0, 1) if 0 <= edge + d < 1 << 53]
     bits = g.integers(1, 54, 1 << 18)
     ms += [int(x) >> (64 - int(b)) for x, b in zip(g.integers(0, 1 << 63, 1 << 18, dtype=np.uint64) << np.uint64(1),
@@ -565,26 +567,25 @@ def pin_neglog64_accuracy(orc):
 
 def pin_neglog64_table(orc):
     """The fixed-point log's constants against their definitions: I_j =
-    2048/(2048 + j) rounded to 11 significant bits, times 2048 (exact
-    rationals); ln(I_j / 2048) and ln 2 each the nearest integer multiple of
-    2^-96 (mpmath, 60 digits), so that E ln 2 + ln inv_j cancels exactly where
-    inv_j = 1/2; the Horner constants 1/k at the scale of S_k: 2^63 for k = 1,
-    2^64 for k = 2, 3 and 2^33 for k = 4 .. 6."""
+    2^23/(2048 + j) rounded up to an integer (exact rationals), so that inv_j =
+    I_j / 4096 is the smallest multiple of 2^-12 at or above 1/(1 + j/2048)
+    and r = M inv_j - 1 lies in [0, 1.5 2^-11) on the whole bin [1 + j/2048,
+    1 + (j + 1)/2048); ln(I_j / 4096) and ln 2 each the nearest integer
+    multiple of 2^-96 (mpmath, 60 digits); the Horner constants 1/k at the
+    scale of S_k: 2^63 for k = 1, 2^64 for k = 2, 3 and 2^33 for k = 4 .. 6."""
     import mpmath as mp
     from fractions import Fraction
     mp.mp.dps = 60
     inv, lninv, ln2, coef = orc.neglog64_table()
-    assert len(inv) == len(lninv) == 2049
-    for j in range(2049):
-        x = Fraction(1 << 22, 2048 + j)  # 2^22/(2048 + j), to be rounded to an integer of 11 significant bits
-        q, rem = divmod(x.numerator, x.denominator)
-        if 2 * rem > x.denominator or (2 * rem == x.denominator and q % 2):
-            q += 1
-        assert inv[j] == q and 1024 <= q <= 2048, j
-        assert lninv[j] == int(mp.nint(mp.log(mp.mpf(inv[j]) / 2048) * mp.mpf(2) ** 96)), j
-    assert inv[0] == 2048 and lninv[0] == 0
+    assert len(inv) == len(lninv) == 2048
+    for j in range(2048):
+        q = -((-(1 << 23)) // (2048 + j))  # ceil(2^23 / (2048 + j))
+        assert inv[j] == q and 2049 <= q <= 4096, j
+        lo, hi = Fraction(2048 + j, 2048), Fraction(2049 + j, 2048)  # the bin of M
+        assert lo * Fraction(q, 4096) - 1 >= 0 and hi * Fraction(q, 4096) - 1 < Fraction(3, 2 ** 12), j
+        assert lninv[j] == int(mp.nint(mp.log(mp.mpf(inv[j]) / 4096) * mp.mpf(2) ** 96)), j
+    assert inv[0] == 4096 and lninv[0] == 0 and inv[2047] == 2049
     assert ln2 == int(mp.nint(mp.log(2) * mp.mpf(2) ** 96))
-    assert lninv[2047] == lninv[2048] == -ln2 and inv[2047] == inv[2048] == 1024 and inv[2046] == 1025
     for k, scale in zip(range(1, 7), (63, 64, 64, 33, 33, 33)):
         assert coef[k] == int(mp.nint(mp.mpf(2) ** scale / k)), k
 
