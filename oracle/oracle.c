@@ -480,8 +480,7 @@ float orc_neglog_f32(uint32_t m)
     float p = fmaf(r, -0x1.99999ap-3f, 0.25f); /* 1/4 - r/5 */
     p = fmaf(r, p, -0x1.555556p-2f);           /* -1/3 + r/4 - r^2/5 */
     p = fmaf(r, p, 0.5f);                      /* 1/2 - r/3 + r^2/4 - r^3/5 */
-    float tail = r2 * p;                       /* -log1p(r) - (-r) */
-    float c = (err + t_lo) + tail;
+    float c = fmaf(r2, p, err + t_lo); /* + the tail r^2 p = -log1p(r) - (-r), in one rounding */
     return s + c;
 }
 

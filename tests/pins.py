@@ -391,7 +391,7 @@ def pin_neglog_f32_exhaustive(orc):
     inputs (tandem-cuda "Performance" and tandem-sycl "Design", Exponentials:
     every draw within 0.571 ulp).  Measured: within 0.5027 ulp (0.5044 without
     the r^5 Taylor term), and the correctly rounded binary32 value on all but
-    98 inputs, where the exact value lies within 0.003 ulp of a rounding
+    82 inputs, where the exact value lies within 0.003 ulp of a rounding
     boundary; u = 0 gives +0 and the top of the grid 23 ln 2 rounded."""
     m, e, ref = _neglog_all(orc)
     nz = ref > 0
