@@ -565,6 +565,22 @@ def pin_neglog64_accuracy(orc):
     assert worst <= 0.5006
 
 
+def pin_neglog64_powers_of_two(orc):
+    """Where 1 - u is a power of two, 2^-k for m = 2^53 - 2^(53 - k), the
+    reduction is exact (M = 1, r = 0) and -ln(1 - u) = k ln 2: the fixed-point
+    log must return k ln 2 correctly rounded (mpmath, 50 digits) for every k
+    in 1 .. 53, and their one-ulp neighbours in m must straddle it."""
+    import mpmath as mp
+    mp.mp.dps = 50
+    ms = np.array([(1 << 53) - (1 << (53 - k)) for k in range(1, 54)], dtype=np.uint64)
+    y = orc.neglog64_array(ms)
+    for k, v in zip(range(1, 54), y):
+        assert v == float(k * mp.log(2)), k
+    below = orc.neglog64_array(ms - np.uint64(1))
+    above = orc.neglog64_array(np.minimum(ms + np.uint64(1), np.uint64((1 << 53) - 1)))
+    assert np.all(below <= y) and np.all(above[:-1] >= y[:-1])
+
+
 def pin_neglog64_table(orc):
     """The fixed-point log's constants against their definitions: I_j =
     2^23/(2048 + j) rounded up to an integer (exact rationals), so that inv_j =
@@ -920,7 +936,7 @@ ALL_PINS = [
     pin_randn_tail_end, pin_randn_distribution, pin_randn_paired, pin_exponentials,
     pin_neglog_f32_exhaustive, pin_neglog_f32_maps_back, pin_neglog_f32_table, pin_exponential_f32_fill,
     pin_cos2pi_exhaustive, pin_cos2pi_coefficients, pin_randn_precise,
-    pin_neglog64_accuracy, pin_neglog64_table, pin_exponential_f64_fill,
+    pin_neglog64_accuracy, pin_neglog64_powers_of_two, pin_neglog64_table, pin_exponential_f64_fill,
     pin_dropout, pin_zexp_zlog,
     pin_zig_table_published, pin_zig_table_invariants, pin_zig_candidate_rounding, pin_zig_miss_rate,
     pin_normal_f64_distribution, pin_zig_wedge_acceptance,
